@@ -1,0 +1,513 @@
+// Persistent, warp-specialised TN GEMM for sm_103a:  D = A x B^T + C  with A (M,K)
+// and B (N,K) K-contiguous ("CuTe 中 A、B 如何加载到 MMA 寄存器", section 1), in
+// FP16 or in the block-scaled NVFP4 / MXFP8 forms ("数据布局及其记号", block-scaled
+// MMA section).
+//
+// One CTA per SM walks output tiles of 128 x BN.  Its warps:
+//   warp 0       TMA producer: per 128-byte K slice, loads the A and B boxes into
+//                128B-swizzled shared memory (and, block-scaled, the raw scale
+//                boxes), arming the stage's `full` barrier with the byte count.
+//   warp 1       MMA issuer (one thread): tcgen05.mma into a TMEM accumulator,
+//                four K steps per stage; tcgen05.commit frees the stage
+//                (`empty`) and, at the end of a tile, hands the accumulator to the
+//                epilogue (`tmem_full`).  Block-scaled: first tcgen05.cp of the
+//                packed scale tiles into TMEM.
+//   warp 2       (block-scaled only) scale-factor packer: rewrites each stage's
+//                row-major scale box, in place, into the 32-lane x 16-byte base
+//                tiles that tcgen05.cp ... .warpx4 copies (local_lane = m % 32,
+//                TCol = m // 32, byte = sfk), then signals `sf_ready`.
+//   warps 4-7    epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//                32*(w%4) .. +31, i.e. rows of the tile), adds C in fp32, rounds
+//                once to fp16 / bf16 and stores 16-byte vectors; then releases
+//                the accumulator buffer (`tmem_empty`).
+// Every wait is bounded: past the limit the kernel records a timeout in the
+// device error word, makes the other warps give up, drains its in-flight copies
+// and MMAs, frees TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace tn {
+
+enum Kind : int { KIND_F16_ACC32 = 0, KIND_F16_ACC16 = 1, KIND_NVFP4 = 2, KIND_MXFP8 = 3 };
+
+// Upper bound on any single pipeline wait; legitimate waits are microseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Bound on the waits of the abandon path (in-flight copies / MMAs).
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+struct Params {
+    int M, N, K;
+    int num_m_blocks, num_n_blocks, num_k_blocks;
+    const void* C;  // [M][N] fp16 (FP16 kinds) or bf16 (block-scaled), or null
+    void* D;        // [M][N], same type as C
+    unsigned int* err;
+};
+
+template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_>
+struct Config {
+    static constexpr int KIND = KIND_;
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int ACC_BUFS = ACC_BUFS_;
+    static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
+    static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
+    // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
+    static constexpr int kKCoordPerStage = (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) ? 64 : 128;
+
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int SFB_GROUPS = kBlockScaled ? (BN + 127) / 128 : 0;  // 128-row scale groups
+    static constexpr int SFA_BYTES = kBlockScaled ? BM * 16 : 0;
+    static constexpr int SFB_BYTES = SFB_GROUPS * 128 * 16;
+    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + (kBlockScaled ? (BM + BN) * 16 : 0);
+
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    // barriers: full[S], empty[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain
+    static constexpr int BAR_FULL = 0;
+    static constexpr int BAR_EMPTY = STAGES;
+    static constexpr int BAR_SF = 2 * STAGES;
+    static constexpr int BAR_TFULL = 3 * STAGES;
+    static constexpr int BAR_TEMPTY = 3 * STAGES + ACC_BUFS;
+    static constexpr int BAR_DRAIN = 3 * STAGES + 2 * ACC_BUFS;
+    static constexpr int NUM_BARS = BAR_DRAIN + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM base address, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+
+    // TMEM: ACC_BUFS accumulators of BN fp32 columns, then the scale-factor slots.
+    static constexpr int SF_COL0 = ACC_BUFS * BN;
+    static constexpr int SF_COLS_PER_COPYSET = 4 * (1 + SFB_GROUPS);  // SFA tile + SFB tiles
+    static constexpr int SF_COLS_PER_STAGE =
+        KIND == KIND_NVFP4 ? kMmasPerStage * SF_COLS_PER_COPYSET
+                           : (KIND == KIND_MXFP8 ? SF_COLS_PER_COPYSET : 0);
+    static constexpr int TMEM_USED = SF_COL0 + STAGES * SF_COLS_PER_STAGE;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                     : TMEM_USED <= 64  ? 64
+                                     : TMEM_USED <= 128 ? 128
+                                     : TMEM_USED <= 256 ? 256
+                                                        : 512;
+    static_assert(TMEM_USED <= 512, "TMEM holds 512 columns");
+    static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per CTA");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
+    static_assert(B_BYTES % 1024 == 0, "B stages stay 1024-byte aligned");
+};
+
+// Output tile -> (m block, n block), grouping 8 m blocks so that concurrently
+// running tiles share A and B panels in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+    constexpr int G = 8;
+    const int per_group = G * num_n;
+    const int g = tile / per_group;
+    const int first_m = g * G;
+    const int gs = min(num_m - first_m, G);
+    const int r = tile - g * per_group;
+    mb = first_m + r % gs;
+    nb = r / gs;
+}
+
+// Bounded parity wait.  Returns false (and stops the other warps) after the
+// time limit, or as soon as another warp has given up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(err, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used only while abandoning work.
+__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kDrainLimitNs) return;
+    }
+}
+
+// Accumulator column -> fp32 value.  FP16 accumulation keeps one element per
+// 32-bit TMEM column, in the low 16 bits.
+template <int KIND>
+__device__ __forceinline__ float acc_value(uint32_t r) {
+    if constexpr (KIND == KIND_F16_ACC16) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(r & 0xFFFFu)));
+    } else {
+        return __uint_as_float(r);
+    }
+}
+
+template <int KIND>
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (KIND == KIND_NVFP4 || KIND == KIND_MXFP8) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+            const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+            const float2 x = __half22float2(h);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+}
+
+template <int KIND>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (KIND == KIND_NVFP4 || KIND == KIND_MXFP8) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        } else {
+            const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One thread's 32 consecutive accumulator columns of one output row:
+// D[row][n .. n+31] = round(acc + C).  N is a multiple of 8.
+template <int KIND>
+__device__ __forceinline__ void store_chunk(const Params& p, int row, int n, const uint32_t (&r)[32]) {
+    if (row >= p.M || n >= p.N) return;
+    const int nvec = min(4, (p.N - n) >> 3);
+    const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
+    const uint16_t* crow = static_cast<const uint16_t*>(p.C) + off;
+    uint16_t* drow = static_cast<uint16_t*>(p.D) + off;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (v < nvec) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
+            if (p.C != nullptr) {
+                float c[8];
+                unpack8<KIND>(*reinterpret_cast<const uint4*>(crow + 8 * v), c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] += c[i];
+            }
+            *reinterpret_cast<uint4*>(drow + 8 * v) = pack8<KIND>(f);
+        }
+    }
+}
+
+// In-place repack of one stage's raw scale box (row r of the box at bytes
+// 16r .. 16r+15, holding sfk = 16c .. 16c+15 for this K range) into the base
+// tiles tcgen05.cp reads: tile (j, h) = scales 4j..4j+3 of rows 128h .. 128h+127,
+// 32 local lanes x 16 bytes, lane l holding rows 128h + l + 32*Mgroup for
+// Mgroup = 0..3 at bytes 4*Mgroup .. 4*Mgroup+3 ("数据布局及其记号": local_lane =
+// m % 32, TCol = m // 32, byte = sfk).  NVFP4: all four words of the box feed
+// the stage's four MMAs, tiles ordered (j, h).  MXFP8: only word `w` (this
+// stage's four scales) is used; one tile per 128-row group.
+template <int GROUPS, bool kAllWords>
+__device__ __forceinline__ void repack_scales(uint8_t* buf, int lane, int w) {
+    uint4* v4 = reinterpret_cast<uint4*>(buf);
+    if constexpr (kAllWords) {
+        uint32_t R[GROUPS][4][4];
+#pragma unroll
+        for (int h = 0; h < GROUPS; ++h)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint4 x = v4[h * 128 + 32 * g + lane];
+                R[h][g][0] = x.x;
+                R[h][g][1] = x.y;
+                R[h][g][2] = x.z;
+                R[h][g][3] = x.w;
+            }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int h = 0; h < GROUPS; ++h)
+                v4[(j * GROUPS + h) * 32 + lane] = make_uint4(R[h][0][j], R[h][1][j], R[h][2][j], R[h][3][j]);
+    } else {
+        const uint32_t* v1 = reinterpret_cast<const uint32_t*>(buf);
+        uint32_t R[GROUPS][4];
+#pragma unroll
+        for (int h = 0; h < GROUPS; ++h)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) R[h][g] = v1[(h * 128 + 32 * g + lane) * 4 + w];
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < GROUPS; ++h) v4[h * 32 + lane] = make_uint4(R[h][0], R[h][1], R[h][2], R[h][3]);
+    }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(256, 1)
+    tn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                   const Params p) {
+    constexpr int KIND = Cfg::KIND;
+    constexpr int BN = Cfg::BN;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int ACC_BUFS = Cfg::ACC_BUFS;
+    constexpr bool kBS = Cfg::kBlockScaled;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + Cfg::OFF_BAR + 8 * i; };
+    volatile uint32_t* tmem_base_slot = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(Cfg::BAR_FULL + s), 1);
+            mbar_init(bar(Cfg::BAR_EMPTY + s), 1);
+            mbar_init(bar(Cfg::BAR_SF + s), 1);
+        }
+        for (int b = 0; b < ACC_BUFS; ++b) {
+            mbar_init(bar(Cfg::BAR_TFULL + b), 1);
+            mbar_init(bar(Cfg::BAR_TEMPTY + b), 128);
+        }
+        mbar_init(bar(Cfg::BAR_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if constexpr (kBS) {
+            tma_prefetch_desc(&tmSFA);
+            tma_prefetch_desc(&tmSFB);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + Cfg::OFF_MISC, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_base_slot;
+
+    const int num_tiles = p.num_m_blocks * p.num_n_blocks;
+    const int nkb = p.num_k_blocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------------- producer
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t loads[STAGES];
+#pragma unroll
+            for (int i = 0; i < STAGES; ++i) loads[i] = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
+                const int m0 = mb * Cfg::BM, n0 = nb * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar(Cfg::BAR_FULL + s);
+                    mbar_arrive_expect_tx(fb, Cfg::TX_BYTES);
+                    const int kx = kb * Cfg::kKCoordPerStage;
+                    tma_load_2d(sbase + Cfg::OFF_A + s * Cfg::A_BYTES, &tmA, fb, kx, m0);
+                    tma_load_2d(sbase + Cfg::OFF_B + s * Cfg::B_BYTES, &tmB, fb, kx, n0);
+                    if constexpr (kBS) {
+                        // 16 scale bytes per row per box; NVFP4 uses all 16 in this stage,
+                        // MXFP8 uses 4 of them (so the same box serves 4 stages).
+                        const int sfx = (KIND == KIND_NVFP4) ? kb * 16 : (kb >> 2) * 16;
+                        tma_load_2d(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, &tmSFA, fb, sfx, m0);
+                        tma_load_2d(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, &tmSFB, fb, sfx, n0);
+                    }
+                    ++loads[s];
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (ok) {
+                // Wait until the consumer has released every stage, so that no
+                // tcgen05.commit arrival is still in flight when the CTA exits.
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) break;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            } else {
+                // Abandoning: let every issued TMA copy land before the CTA exits.
+                for (int i = 0; i < STAGES; ++i)
+                    if (loads[i] > 0) wait_bar_drain(bar(Cfg::BAR_FULL + i), (loads[i] - 1u) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------------------------------------------------- MMA issuer
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            int t_local = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t_local) {
+                const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
+                const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
+                if (!wait_bar(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if constexpr (kBS) {
+                        if (!wait_bar(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t adesc = smem_desc_sw128(sbase + Cfg::OFF_A + s * Cfg::A_BYTES);
+                    const uint64_t bdesc = smem_desc_sw128(sbase + Cfg::OFF_B + s * Cfg::B_BYTES);
+                    if constexpr (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) {
+                        constexpr uint32_t idesc = idesc_f16(128, BN, KIND == KIND_F16_ACC32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                    } else {
+                        const uint32_t sfa_smem = sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
+                        const uint32_t sfb_smem = sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
+                        const uint32_t sf_tmem =
+                            tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
+                        if constexpr (KIND == KIND_NVFP4) {
+                            constexpr uint32_t idesc = idesc_block_scaled(128, BN, 1u, false, 0u);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t sfa_t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
+                                const uint32_t sfb_t = sfa_t + 4;
+                                tmem_cp_32x128b_warpx4(sfa_t, smem_desc_sf_tile(sfa_smem + j * 512));
+#pragma unroll
+                                for (int h = 0; h < Cfg::SFB_GROUPS; ++h)
+                                    tmem_cp_32x128b_warpx4(
+                                        sfb_t + 4 * h, smem_desc_sf_tile(sfb_smem + (j * Cfg::SFB_GROUPS + h) * 512));
+                                mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t, sfb_t,
+                                                (kb | j) != 0);
+                            }
+                        } else {
+                            const uint32_t sfa_t = sf_tmem;
+                            const uint32_t sfb_t = sf_tmem + 4;
+                            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_sf_tile(sfa_smem));
+#pragma unroll
+                            for (int h = 0; h < Cfg::SFB_GROUPS; ++h)
+                                tmem_cp_32x128b_warpx4(sfb_t + 4 * h, smem_desc_sf_tile(sfb_smem + h * 512));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j,
+                                                idesc_block_scaled(128, BN, 0u, true, static_cast<uint32_t>(j)),
+                                                sfa_t, sfb_t, (kb | j) != 0);
+                        }
+                    }
+                    tc_commit(bar(Cfg::BAR_EMPTY + s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(bar(Cfg::BAR_TFULL + buf));
+            }
+            if (!ok) {
+                // Abandoning: wait for the MMAs and copies already issued.
+                tc_commit(bar(Cfg::BAR_DRAIN));
+                wait_bar_drain(bar(Cfg::BAR_DRAIN), 0u);
+            }
+        }
+    } else if (warp == 2) {
+        if constexpr (kBS) {
+            // -------------------------------------------------------------- scale packer
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err));
+                    if (!ok) break;
+                    uint8_t* sfa = smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
+                    uint8_t* sfb = smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
+                    if constexpr (KIND == KIND_NVFP4) {
+                        repack_scales<1, true>(sfa, lane, 0);
+                        repack_scales<Cfg::SFB_GROUPS, true>(sfb, lane, 0);
+                    } else {
+                        repack_scales<1, false>(sfa, lane, kb & 3);
+                        repack_scales<Cfg::SFB_GROUPS, false>(sfb, lane, kb & 3);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(Cfg::BAR_SF + s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int t_local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_local) {
+            const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
+            const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
+            const bool ok =
+                __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
+            if (!ok) break;
+            tc_fence_after_sync();
+            int mb, nb;
+            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
+            const int row = mb * Cfg::BM + q * 32 + lane;
+            const int n0 = nb * BN;
+            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                if (n0 + c >= p.N) break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), r);
+                tmem_ld_wait();
+                store_chunk<KIND>(p, row, n0 + c, r);
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace tn

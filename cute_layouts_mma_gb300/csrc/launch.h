@@ -1,0 +1,38 @@
+// Host-side glue shared by the C-ABI (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tn_gemm.h"
+
+namespace tn {
+
+// Encode a 2-D tiled TMA map over a row-major matrix: `inner` elements per row
+// (contiguous), `rows` rows `pitch` bytes apart, boxes of box_inner x box_rows.
+// swizzle128: 128-byte XOR swizzle in shared memory (box rows of 128 bytes).
+// Returns false if the driver rejects the map.
+bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                   uint64_t rows, uint64_t pitch, uint32_t box_inner, uint32_t box_rows,
+                   bool swizzle128);
+
+// Launchers; arguments are already validated.  `sms` is the SM count of the
+// current device, `dev` its ordinal.
+gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                              const void* C, void* D, int accum, cudaStream_t stream, int sms,
+                              int dev);
+gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void* A,
+                                       const void* SFA, const void* B, const void* SFB,
+                                       const void* C, void* D, int fmt, cudaStream_t stream,
+                                       int sms, int dev);
+
+// Read and clear the device error word of each kernel family on the current
+// device (synchronous).  Non-zero means a kernel abandoned its work.
+unsigned int read_clear_error_f16();
+unsigned int read_clear_error_block_scaled();
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace tn

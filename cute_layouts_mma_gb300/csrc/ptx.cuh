@@ -1,0 +1,231 @@
+// Inline-PTX wrappers for sm_103a: mbarrier, TMA tensor loads, tcgen05 (TMEM
+// allocation, MMA, scale-factor copy, loads) and the shared-memory / instruction
+// descriptors the tcgen05 MMA reads.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>  // CUtensorMap
+
+namespace tn {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make initialised barriers visible to the async proxy (TMA, tcgen05).
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (tcgen05.cp, TMA store).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ TMA
+
+// 2-D tiled load of one box into shared memory; completion is signalled on `bar`
+// as transaction bytes.  x is the innermost (contiguous) coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+// Allocate `ncols` TMEM columns (power of two >= 32); the address lands in smem.
+// Executed by one full warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// (MMAs, copies) has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+// D(tmem) = A(smem) x B(smem)^T (+ D if accumulate), FP16/BF16 inputs.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Block-scaled MMA, FP8 operands, one scale per 32 K (scale_vec::1X).
+__device__ __forceinline__ void mma_mxf8f6f4_1x(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Block-scaled MMA, packed FP4 operands, one E4M3 scale per 16 K (scale_vec::4X).
+__device__ __forceinline__ void mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy a 32-row x 16-byte shared-memory tile into TMEM at `taddr` (32 lanes x 4
+// columns) and replicate it to all four 32-lane partitions (.warpx4).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// Each thread of the warp reads 32 consecutive 32-bit columns of its own TMEM
+// lane (lane = 32 * (warp % 4) + laneid).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ descriptors
+
+// Shared-memory matrix descriptor, K-major operand tile of 128-byte rows written
+// by TMA with the 128-byte swizzle: 8-row x 128-byte atoms (1024 bytes) stacked
+// along M/N, so the stride between 8-row groups is 1024 bytes.  The 16-byte
+// sector s of row r sits at sector s ^ (r % 8) ("数据布局及其记号", section
+// "Swizzle Layout").  Stepping K inside the 128-byte row adds bytes to the start
+// address; the tile base is 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // bits 0-13: start address / 16
+    d |= static_cast<uint64_t>(1) << 16;                   // bits 16-29: leading offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // bits 32-45: 8-row group stride
+    d |= static_cast<uint64_t>(1) << 46;                   // bits 46-47: descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                   // bits 61-63: 128-byte swizzle
+    return d;
+}
+
+// Shared-memory descriptor of a plain (unswizzled) 32-row x 16-byte tile, rows
+// 16 bytes apart: four 8-row core matrices of 128 bytes each.
+__device__ __forceinline__ uint64_t smem_desc_sf_tile(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128 >> 4) << 16;  // leading offset: next core matrix along K
+    d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride offset: next 8-row core matrix
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;  // layout type 0: no swizzle
+}
+
+// Instruction descriptor, kind::f16: FP16 A and B, both K-major; D in fp32
+// (d_f32) or fp16; M x N tile.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool d_f32) {
+    return (d_f32 ? 1u : 0u) << 4          // D format: 0 = F16, 1 = F32
+           | 0u << 7                       // A format: F16
+           | 0u << 10                      // B format: F16
+           | 0u << 15 | 0u << 16           // A, B K-major
+           | static_cast<uint32_t>(n >> 3) << 17
+           | static_cast<uint32_t>(m >> 4) << 24;
+}
+
+// Instruction descriptor for block-scaled kinds.  ab_format: 0 = E4M3 under
+// kind::mxf8f6f4, 1 = E2M1 under kind::mxf4nvf4.  scale_e8m0: scale type UE8M0
+// (else UE4M3).  sf_id selects the byte of each 32-bit scale column (scale_vec 1X).
+__host__ __device__ constexpr uint32_t idesc_block_scaled(int m, int n, uint32_t ab_format,
+                                                          bool scale_e8m0, uint32_t sf_id) {
+    return (sf_id & 3u) << 4                       // B scale-factor byte
+           | ab_format << 7 | ab_format << 10      // A, B formats
+           | 0u << 15 | 0u << 16                   // K-major
+           | static_cast<uint32_t>(n >> 3) << 17
+           | (scale_e8m0 ? 1u : 0u) << 23
+           | static_cast<uint32_t>(m >> 4) << 24
+           | (sf_id & 3u) << 29;                   // A scale-factor byte
+}
+
+}  // namespace tn

@@ -1,0 +1,118 @@
+/*
+ * tn_gemm.h -- C ABI of the GB300 (sm_103a) TN matrix multiply-accumulate library.
+ *
+ *   D = A x B + C,  A indexed (M,K), B indexed (N,K), both K-contiguous ("TN").
+ *
+ * Source of the operation:
+ *   - "CuTe 中 A、B 如何加载到 MMA 寄存器", section 1: D = A x B + C with A
+ *     indexed (M,K) and B indexed (N,K), K contiguous in both; C and D are M x N.
+ *     The pages' FP16-in / FP16-accumulate atom (F16F16F16F16_TN) and the FP32-
+ *     accumulate variant are the two accumulation modes of gemm_f16.
+ *   - "数据布局及其记号", section on block-scaled MMA (TMEM scale factors):
+ *     A_real[m,k] = A_low[m,k] * SFA[m, k // K_blk], likewise B with SFB[n, .],
+ *     D = C + A_real x B_real; NVFP4 = E2M1 data + one E4M3 scale per 16
+ *     K-elements, MXFP8 = E4M3 data + one E8M0 scale per 32 K-elements.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *     library never frees, keeps or allocates device memory for a call.
+ *   - Matrices are dense and row-major with no padding: A rows are K elements
+ *     long (NVFP4: K/2 bytes), B rows likewise, C and D rows are N elements.
+ *     Scale-factor matrices are row-major u8 [rows][K / K_blk].
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and do not synchronise.  Arguments are checked on the host before
+ *     anything is launched; a rejected call launches nothing.
+ *   - D must not overlap A, B, SFA or SFB.  D may be exactly C (in place), or
+ *     disjoint from it; a partial overlap is rejected.
+ *   - All pointers must be 16-byte aligned.  Row pitches must be multiples of
+ *     16 bytes (see each call).  M and N need not be multiples of any tile.
+ *   - Device-side failures (a pipeline wait that exceeds its time limit) do not
+ *     hang or fault the GPU: the kernel abandons its work, records the failure
+ *     and returns; gemm_last_device_error() reports it.
+ *   - Calls may be made from several host threads; the library's only state is
+ *     per-device, set up on first use (kernel attributes, SM count).
+ *
+ * Numerics: products are formed by the tensor cores
+ * and summed in fp32 (GEMM_ACC_F32) or fp16 (GEMM_ACC_F16); C is added in fp32
+ * and the result rounded once, to nearest even, to the output type.
+ */
+#ifndef TN_GEMM_H
+#define TN_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __DRIVER_TYPES_H__
+typedef struct CUstream_st *cudaStream_t;
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* a size, enum or pointer argument is out of range  */
+    GEMM_ERR_UNSUPPORTED = 2, /* no GPU of compute capability 10.3 is current      */
+    GEMM_ERR_ALIGNMENT = 3,   /* a pointer or a row pitch is not 16-byte aligned   */
+    GEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
+    GEMM_ERR_TIMEOUT = 5      /* a kernel gave up on a pipeline wait (device side) */
+} gemm_status_t;
+
+enum { GEMM_ACC_F32 = 0, GEMM_ACC_F16 = 1 };   /* accum_dtype of gemm_f16        */
+enum { GEMM_FMT_NVFP4 = 0, GEMM_FMT_MXFP8 = 1 }; /* fmt of gemm_block_scaled      */
+
+/*
+ * FP16 TN GEMM:  D[m][n] = round_fp16( C[m][n] + sum_k A[m][k] * B[n][k] ).
+ *
+ *   M, N, K      sizes, each >= 1 and < 2^31.  K % 8 == 0 and N % 8 == 0 (16-byte
+ *                row pitches for A, B, C, D).
+ *   A            half[M][K], K contiguous.
+ *   B            half[N][K], K contiguous.
+ *   C            half[M][N] or NULL (NULL: C = 0, nothing is read).
+ *   D            half[M][N], written; may equal C.
+ *   accum_dtype  GEMM_ACC_F32: tensor-core sums in fp32.
+ *                GEMM_ACC_F16: tensor-core sums in fp16 (the pages' F16F16F16F16
+ *                atom); C is then added in fp32 before the final rounding.
+ *   stream       cudaStream_t the kernel is launched on.
+ * Returns GEMM_OK once the kernel is enqueued, else the first failed check.
+ */
+gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                       const void *C, void *D, int accum_dtype, cudaStream_t stream);
+
+/*
+ * Block-scaled TN GEMM:
+ *   D[m][n] = round_bf16( C[m][n] + sum_k (A[m][k] * SFA[m][k/K_blk])
+ *                                         * (B[n][k] * SFB[n][k/K_blk]) ).
+ *
+ *   fmt == GEMM_FMT_NVFP4: K_blk = 16.  A is u8[M][K/2] holding two E2M1 codes
+ *        per byte, element 2j in the low nibble and 2j+1 in the high nibble of
+ *        byte j.  SFA is u8[M][K/16] of E4M3 scales; the sign bit must be 0
+ *        (the tensor cores read the scale as unsigned E4M3).  K % 256 == 0.
+ *   fmt == GEMM_FMT_MXFP8: K_blk = 32.  A is u8[M][K] of E4M3 codes.  SFA is
+ *        u8[M][K/32] of E8M0 exponents (value 2^(e-127)).  K % 512 == 0.
+ *   B, SFB       the same layouts with N rows.
+ *   C            bf16[M][N] or NULL (NULL: C = 0, nothing is read).
+ *   D            bf16[M][N], written; may equal C.  N % 8 == 0.
+ * The K multiples make every scale-factor row a whole number of 16-byte
+ * chunks.  Sums are fp32.  NaN scales or data give undefined (finite or NaN)
+ * results in the affected outputs; no other effect.
+ */
+gemm_status_t gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void *A,
+                                const void *SFA, const void *B, const void *SFB,
+                                const void *C, void *D, int fmt, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *gemm_status_string(gemm_status_t status);
+
+/*
+ * Synchronises the current device, then returns GEMM_ERR_TIMEOUT if any kernel
+ * of this library abandoned its work since the previous call (and clears that
+ * record), GEMM_ERR_CUDA if the device reports an error, else GEMM_OK.
+ */
+gemm_status_t gemm_last_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TN_GEMM_H */

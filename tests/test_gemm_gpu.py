@@ -1,0 +1,200 @@
+"""GPU parity of the CUDA TN GEMM against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import cute_layouts_mma_gb300 as tg
+from cute_layouts_mma_gb300 import inputs
+import oracle
+
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tg.lib()
+
+
+# ------------------------------------------------------------------ FP16, fp32 accumulation
+
+def test_fp16_int_256_bit_exact():
+    prob = inputs.workload_problem("fp16_int_256")
+    D = P.run_gpu(prob, accum=0)
+    P.check(prob, D, mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (128, 256, 64), (130, 264, 72), (300, 520, 200),
+                                   (257, 8, 1000), (64, 1000, 4096), (1000, 16, 520)])
+def test_fp16_ragged_shapes_tolerance(M, N, K):
+    prob = inputs.make_problem("f16", M, N, K, seed=M + N + K, dist="normal0.1", with_c=True)
+    D = P.run_gpu(prob, accum=0)
+    P.check(prob, D, mode="tol")
+
+
+def test_fp16_integers_with_c_bit_exact():
+    prob = inputs.make_problem("f16", 384, 520, 512, seed=7, dist="int2", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), mode="exact")
+
+
+def test_fp16_in_place_and_null_c():
+    prob = inputs.make_problem("f16", 200, 264, 136, seed=8, dist="int2", with_c=True)
+    dev = P.device()
+    g = P.to_device(prob, dev)
+    D = g["C"].clone()
+    tg.gemm_f16(g["A"], g["B"], D, D, tg.GEMM_ACC_F32)  # D is C
+    torch.cuda.synchronize()
+    P.check(prob, D.cpu(), mode="exact")
+    prob0 = dict(prob, C=None)
+    D0 = P.run_gpu(prob0, accum=0)
+    Dz = P.run_gpu(dict(prob, C=torch.zeros_like(prob["C"])), accum=0)
+    assert torch.equal(D0.view(torch.int16), Dz.view(torch.int16))
+    P.check(prob0, D0, mode="exact")
+
+
+def test_fp16_guard_bands_untouched():
+    prob = inputs.make_problem("f16", 130, 136, 64, seed=9, dist="int2", with_c=False)
+    M, N = 130, 136
+    pad = 4096
+    dev = P.device()
+    buf = torch.full((M * N + 2 * pad,), float("nan"), dtype=torch.float16, device=dev)
+    D = buf[pad:pad + M * N].view(M, N)
+    P.run_gpu(prob, accum=0, D=D)
+    host = buf.cpu()
+    assert torch.isnan(host[:pad]).all() and torch.isnan(host[pad + M * N:]).all()
+    P.check(prob, D.cpu(), mode="exact")
+
+
+def test_fp16_side_stream():
+    prob = inputs.make_problem("f16", 256, 512, 256, seed=10, dist="int2", with_c=True)
+    s = torch.cuda.Stream()
+    D = P.run_gpu(prob, accum=0, stream=s)
+    P.check(prob, D, mode="exact")
+
+
+def test_fp16_4096_full_size_sampled_rows():
+    prob = inputs.workload_problem("fp16_4096")
+    D = P.run_gpu(prob, accum=0)
+    rows = P.sample_rows(prob["M"], 32, seed=1)
+    info = P.check(prob, D, rows=rows, mode="tol")
+    # the stated bound, output rounding included, without the extra half ulp
+    d16, d64 = P.oracle_result(prob, rows)
+    assert float(np.max(np.abs(D[rows].double().numpy() - d64))) <= P.tolerance_f32acc(prob)
+    # properties at every row: finite, and equal to the same launch repeated
+    assert torch.isfinite(D.float()).all()
+    D2 = P.run_gpu(prob, accum=0)
+    assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+
+
+# ------------------------------------------------------------------ FP16 accumulation
+
+def test_fp16acc_integers_bit_exact():
+    # every partial sum is an integer of magnitude <= 1024: exact in fp16
+    prob = inputs.make_problem("f16", 256, 264, 256, seed=11, dist="int2", with_c=False)
+    P.check(prob, P.run_gpu(prob, accum=1), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (200, 136, 328)])
+def test_fp16acc_frobenius(M, N, K):
+    prob = inputs.make_problem("f16", M, N, K, seed=12, dist="uniform0.5", with_c=False)
+    P.check(prob, P.run_gpu(prob, accum=1), mode="fro")
+
+
+def test_fp16acc_8192x1024_full_size_sampled_rows():
+    prob = inputs.workload_problem("fp16acc_8192x1024")
+    D = P.run_gpu(prob, accum=1)
+    rows = P.sample_rows(prob["M"], 48, seed=2)
+    P.check(prob, D, rows=rows, mode="fro")
+    assert torch.isfinite(D.float()).all()
+
+
+# ------------------------------------------------------------------ NVFP4
+
+@pytest.mark.parametrize("with_c", [False, True])
+def test_nvfp4_integers_bit_exact(with_c):
+    prob = inputs.make_problem("nvfp4", 256, 512, 512, seed=13, dist="int", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 264, 768), (129, 8, 256), (384, 1024, 2048)])
+def test_nvfp4_random_tolerance(M, N, K):
+    prob = inputs.make_problem("nvfp4", M, N, K, seed=M + K, dist="codes", with_c=True)
+    P.check(prob, P.run_gpu(prob), mode="tol")
+
+
+def _one_hot_problem(kind, M, N, K, row, col, sfk):
+    kblk = 16 if kind == "nvfp4" else 32
+    if kind == "nvfp4":
+        A = torch.full((M, K // 2), 0x22, dtype=torch.uint8)
+        B = torch.full((N, K // 2), 0x22, dtype=torch.uint8)
+        s1, s2 = 0x38, 0x40
+    else:
+        A = torch.full((M, K), 0x38, dtype=torch.uint8)
+        B = torch.full((N, K), 0x38, dtype=torch.uint8)
+        s1, s2 = 127, 128
+    SFA = torch.full((M, K // kblk), s1, dtype=torch.uint8)
+    SFB = torch.full((N, K // kblk), s1, dtype=torch.uint8)
+    if row is not None:
+        SFA[row, sfk] = s2
+    if col is not None:
+        SFB[col, sfk] = s2
+    return {"kind": kind, "M": M, "N": N, "K": K, "A": A, "B": B, "SFA": SFA, "SFB": SFB, "C": None}
+
+
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp8"])
+@pytest.mark.parametrize("row,col,sfk", [(0, None, 0), (37, None, 5), (None, 200, 6),
+                                         (127, 129, 15), (64, None, 2), (None, 31, 3)])
+def test_one_hot_scale_probe(kind, row, col, sfk):
+    """All data 1 and all scales 1 except one SFA row or SFB column block set to 2:
+    only that row / column of D moves, by K_blk."""
+    prob = _one_hot_problem(kind, 256, 264, 1024, row, col, sfk)
+    D = P.run_gpu(prob)
+    P.check(prob, D, mode="exact")
+
+
+# ------------------------------------------------------------------ MXFP8
+
+@pytest.mark.parametrize("with_c", [False, True])
+def test_mxfp8_integers_bit_exact(with_c):
+    prob = inputs.make_problem("mxfp8", 128, 256, 1024, seed=14, dist="int", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 392, 1024), (128, 136, 512), (64, 2048, 4096)])
+def test_mxfp8_random_tolerance(M, N, K):
+    prob = inputs.make_problem("mxfp8", M, N, K, seed=M + N, dist="normal", with_c=True)
+    P.check(prob, P.run_gpu(prob), mode="tol")
+
+
+def test_nvfp4_8192_full_size_sampled_rows():
+    prob = inputs.workload_problem("nvfp4_8192")
+    D = P.run_gpu(prob)
+    rows = P.sample_rows(prob["M"], 16, seed=3)
+    P.check(prob, D, rows=rows, mode="tol")
+    assert torch.isfinite(D.float()).all()
+
+
+def test_mxfp8_128x16384_full_size_sampled_rows():
+    prob = inputs.workload_problem("mxfp8_128x16384")
+    D = P.run_gpu(prob)
+    rows = P.sample_rows(prob["M"], 16, seed=4)
+    P.check(prob, D, rows=rows, mode="tol")
+    assert torch.isfinite(D.float()).all()
+
+
+# ------------------------------------------------------------------ argument errors on the GPU
+
+def test_misaligned_output_is_rejected_not_faulted():
+    dev = P.device()
+    A = torch.zeros(64, 64, dtype=torch.float16, device=dev)
+    B = torch.zeros(64, 64, dtype=torch.float16, device=dev)
+    buf = torch.zeros(64 * 64 + 8, dtype=torch.float16, device=dev)
+    D = buf[1:1 + 64 * 64].view(64, 64)
+    with pytest.raises(tg.GemmError) as ei:
+        tg.gemm_f16(A, B, None, D)
+    assert ei.value.code == tg.GEMM_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert tg.gemm_last_device_error() == tg.GEMM_OK
