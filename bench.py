@@ -1,0 +1,433 @@
+"""Benchmark of the GB300 TN GEMM (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one GEMM over one synthetic problem of the named workload (default:
+the FP16 M=N=K=4096 GEMM with fp32 accumulation and C).  Inputs live in HBM before
+timing starts; successive steps rotate through enough input/output sets that
+each step's operands were evicted from L2 by the others.  Under torchrun each
+rank runs its own independent problem on its own GPU (weak scaling, no
+collective on the data path); the reported value is all ranks' FLOPs over the
+slowest rank's time.
+
+--impl reference times the CPU oracle (the deliberately slow fp64 reference) on
+a bounded row sample of the same workload per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense tensor rates relative to bf16 (2.25 PF): fp8 4.5 PF, fp4 13.5 PF
+NOMINAL_RATIO = {"f16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
+METRIC = "GEMM TFLOPS (FP16 TN, NVFP4/MXFP8 block-scaled) and % of dense tensor peak"
+KERNEL_SOURCES = ["cute_layouts_mma_gb300/csrc/gemm_kernel.cuh", "cute_layouts_mma_gb300/csrc/ptx.cuh",
+                  "cute_layouts_mma_gb300/csrc/gemm_f16.cu", "cute_layouts_mma_gb300/csrc/gemm_bs.cu"]
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def workload_bytes(w) -> int:
+    """Algorithmic HBM bytes of one launch: read A, B, scales, C once; write D once."""
+    if w.kind == "f16":
+        ab = 2 * (w.M + w.N) * w.K
+        sf = 0
+    elif w.kind == "nvfp4":
+        ab = (w.M + w.N) * w.K // 2
+        sf = (w.M + w.N) * w.K // 16
+    else:
+        ab = (w.M + w.N) * w.K
+        sf = (w.M + w.N) * w.K // 32
+    c = 2 * w.M * w.N if w.with_c else 0
+    return ab + sf + c + 2 * w.M * w.N
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU is busy."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "util": float(f[4]),
+                             "hw": f[6], "hwt": f[7], "swt": f[8], "pcap": f[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        busy = [r for r in rows if r["util"] > 50] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["max"] for r in busy),
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class GemmRunner:
+    """Device-resident rotating problem sets for one workload, plus the launch call."""
+
+    def __init__(self, w, dev, sets: int):
+        import torch
+        import cute_layouts_mma_gb300 as tg
+        from cute_layouts_mma_gb300 import inputs
+        self.w, self.dev, self.tg = w, dev, tg
+        base = inputs.make_problem(w.kind, w.M, w.N, w.K, w.seed, w.dist, w.with_c)
+        self.host = base
+        out_dtype = torch.float16 if w.kind == "f16" else torch.bfloat16
+        first = {k: (base[k].to(dev) if base.get(k) is not None else None) for k in ("A", "B", "C", "SFA", "SFB")}
+        self.sets = []
+        for i in range(sets):
+            s = {k: (v if i == 0 or v is None else v.clone()) for k, v in first.items()}
+            s["D"] = torch.empty(w.M, w.N, dtype=out_dtype, device=dev)
+            self.sets.append(s)
+        self.fmt = tg.GEMM_FMT_NVFP4 if w.kind == "nvfp4" else tg.GEMM_FMT_MXFP8
+
+    def launch(self, i: int, stream=None):
+        s = self.sets[i % len(self.sets)]
+        if self.w.kind == "f16":
+            self.tg.gemm_f16(s["A"], s["B"], s["C"], s["D"], self.w.accum, stream)
+        else:
+            self.tg.gemm_block_scaled(s["A"], s["SFA"], s["B"], s["SFB"], s["C"], s["D"], self.fmt, stream)
+
+
+def rotating_sets(w) -> int:
+    ws = workload_bytes(w)
+    return min(1024, max(2, math.ceil(3 * L2_BYTES / ws) + 1)) if ws < 3 * L2_BYTES else 2
+
+
+def time_steps(runner, steps: int, stream) -> float:
+    """Milliseconds for `steps` back-to-back launches, CUDA events on `stream`."""
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            runner.launch(i, stream)
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def peak_for(w, peaks):
+    """(bound, peak, unit) of the workload's kernel."""
+    if w.kind == "mxfp8" and w.M <= 128:
+        return "hbm", peaks["hbm_gbs"], "GB/s"
+    return "tensor", peaks["bf16_tflops"] * NOMINAL_RATIO[w.kind], "TFLOP/s"
+
+
+def roofline(w, ms_per_launch, peaks, peak_src):
+    bound, peak, unit = peak_for(w, peaks)
+    if bound == "hbm":
+        achieved = workload_bytes(w) / (ms_per_launch * 1e-3) / 1e9
+    else:
+        achieved = w.flops / (ms_per_launch * 1e-3) / 1e12
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+            "peak_source": peak_src + (" (bf16 x nominal dtype ratio)" if w.kind == "nvfp4" or
+                                       (w.kind == "mxfp8" and bound == "tensor") else ""),
+            "algorithmic_bytes": workload_bytes(w), "algorithmic_flops": w.flops}
+
+
+def e2e_measure(runner, steps: int, stream):
+    """Same metric through the public call with host buffers: per step, pinned host ->
+    device copies of the step's inputs, the GEMM, and a device -> host read of D."""
+    import torch
+    w, s = runner.w, runner.sets[0]
+    names = [k for k in ("A", "B", "SFA", "SFB", "C") if s.get(k) is not None]
+    host_in = {k: runner.host[k].pin_memory() for k in names}
+    host_out = torch.empty(s["D"].shape, dtype=s["D"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for it in range(steps + 1):
+            if it == 1:
+                start.record(stream)
+            for k in names:
+                s[k].copy_(host_in[k], non_blocking=True)
+            runner.launch(0, stream)
+            host_out.copy_(s["D"], non_blocking=True)
+        end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w, budget_s: float):
+    """The oracle, as it stands, on a row sample of the workload; TFLOP/s."""
+    import numpy as np
+    import oracle
+    from cute_layouts_mma_gb300 import inputs
+    p = inputs.make_problem(w.kind, w.M, w.N, w.K, w.seed, w.dist, w.with_c)
+
+    def run(rows):
+        t0 = time.perf_counter()
+        if w.kind == "f16":
+            oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows)
+        else:
+            fmt = oracle.NVFP4 if w.kind == "nvfp4" else oracle.MXFP8
+            oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows)
+        return time.perf_counter() - t0
+
+    threads = oracle.num_threads()
+    probe_rows = list(range(min(w.M, threads)))
+    t_probe = run(probe_rows)
+    per_row = t_probe / len(probe_rows)
+    nrows = int(min(w.M, max(len(probe_rows), budget_s / per_row)))
+    rng = np.random.default_rng(0)
+    rows = sorted(rng.choice(w.M, size=nrows, replace=False).tolist())
+    t = run(rows)
+    tflops = 2.0 * nrows * w.N * w.K / t / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nrows} of {w.M} output rows (all N columns), fp64 oracle, {t:.1f} s"}, t
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+    from cute_layouts_mma_gb300 import inputs
+    rank, local_rank, world = env_rank()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = inputs.WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    runner = GemmRunner(w, dev, rotating_sets(w))
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with ClockSampler(local_rank) as clocks:
+        for i in range(args.warmup):
+            with torch.cuda.stream(stream):
+                runner.launch(i, stream)
+        torch.cuda.synchronize()
+        # extra untimed warm-up so the clocks settle and the sampler sees load
+        t0 = time.perf_counter()
+        while not args.quick and time.perf_counter() - t0 < 1.0:
+            time_steps(runner, 20, stream)
+        barrier()
+        torch.cuda.synchronize()
+        ms_total = time_steps(runner, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert runner.tg.gemm_last_device_error() == runner.tg.GEMM_OK
+
+    if args.quick:  # profiling runs: only the W + K launches above
+        if rank == 0:
+            print(json.dumps({"quick": True, "workload": w.name, "ms_per_step": ms,
+                              "tflops": world * w.flops / (ms * 1e-3) / 1e12}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    e2e_ms, h2d, d2h = e2e_measure(runner, max(3, min(args.steps, 20)), stream)
+    value = world * w.flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"f16": "f16" if w.accum == 0 else "f16 (f16 accumulate)", "nvfp4": "nvfp4 (e2m1+e4m3/16)",
+                  "mxfp8": "mxfp8 (e4m3+e8m0/32)"}[w.kind],
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "with_c": w.with_c,
+                   "accum": "f32" if w.accum == 0 else "f16",
+                   "l2": f"{len(runner.sets)} rotating input/output sets ({workload_bytes(w) * len(runner.sets) >> 20} MiB) so every step's operands are cold in L2",
+                   "parallelism": f"independent problem per GPU x{world}"},
+        "roofline": roofline(w, ms, peaks, peak_src),
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_extras:
+        extras = {}
+        for name, ww in inputs.WORKLOADS.items():
+            if name == w.name:
+                continue
+            r = GemmRunner(ww, dev, rotating_sets(ww))
+            for i in range(3):
+                r.launch(i, stream)
+            torch.cuda.synchronize()
+            n = 30 if ww.flops > 1e10 else 200
+            mse = time_steps(r, n, stream) / n
+            extras[name] = {"ms": round(mse, 5), "tflops": round(ww.flops / (mse * 1e-3) / 1e12, 2),
+                            "roofline": roofline(ww, mse, peaks, peak_src)}
+            del r
+            torch.cuda.empty_cache()
+        assert runner.tg.gemm_last_device_error() == runner.tg.GEMM_OK
+        line["per_workload"] = extras
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb, _ = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def reference_arm(args):
+    """The CPU oracle as the reference implementation, timed per step on a row sample."""
+    rank, _, world = env_rank()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from cute_layouts_mma_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    p = inputs.make_problem(w.kind, w.M, w.N, w.K, w.seed, w.dist, w.with_c)
+    threads = oracle.num_threads()
+
+    def run(rows):
+        if w.kind == "f16":
+            oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows)
+        else:
+            fmt = oracle.NVFP4 if w.kind == "nvfp4" else oracle.MXFP8
+            oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows)
+
+    probe = list(range(min(w.M, threads)))
+    t0 = time.perf_counter()
+    run(probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    total_steps = args.steps + args.warmup
+    rows_per_step = int(max(1, min(w.M, args.reference_seconds / total_steps / per_row)))
+    rng = np.random.default_rng(0)
+    samples = [sorted(rng.choice(w.M, size=rows_per_step, replace=False).tolist()) for _ in range(total_steps)]
+    for i in range(args.warmup):
+        run(samples[i])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run(samples[args.warmup + i])
+    t = time.perf_counter() - t0
+    ms = t * 1e3 / args.steps
+    value = 2.0 * rows_per_step * w.N * w.K / (ms * 1e-3) / 1e12
+    sample = f"{rows_per_step} of {w.M} output rows per step (all N columns), fp64 oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="fp16_4096")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling mode: only W warm-up and K timed launches, short JSON line")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of cpu_baseline")
+    ap.add_argument("--reference-seconds", type=float, default=90.0,
+                    help="oracle time budget of the whole --impl reference run")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
