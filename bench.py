@@ -266,6 +266,22 @@ def cpu_baseline(w, budget_s: float):
             "sample": f"{nrows} of {w.M} output rows (all N columns), fp64 oracle, {t:.1f} s"}, t
 
 
+def reduce_max(value: float, world: int, device) -> float:
+    """Max of a per-rank value over all ranks (the slowest rank's step time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -298,11 +314,7 @@ def gpu_arm(args):
         ms_total = time_steps(runner, args.steps, stream)
         torch.cuda.synchronize()
         barrier()
-    ms = ms_total / args.steps
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms_total / args.steps, world, dev)
     assert runner.tg.gemm_last_device_error() == runner.tg.GEMM_OK
 
     if args.quick:  # profiling runs: only the W + K launches above
@@ -313,7 +325,7 @@ def gpu_arm(args):
             dist.destroy_process_group()
         return
     e2e_ms, h2d, d2h = e2e_measure(runner, max(3, min(args.steps, 20)), stream)
-    value = world * w.flops / (ms * 1e-3) / 1e12
+    value = job_value(world, w.flops, ms)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
