@@ -179,10 +179,27 @@ def rotating_sets(w) -> int:
     return min(1024, max(2, math.ceil(3 * L2_BYTES / ws) + 1)) if ws < 3 * L2_BYTES else 2
 
 
-def time_steps(runner, steps: int, stream) -> float:
-    """Milliseconds for `steps` back-to-back launches, CUDA events on `stream`."""
+def time_steps(runner, steps: int, stream, graph: bool = True) -> float:
+    """Milliseconds for `steps` back-to-back launches, CUDA events on `stream`.
+
+    With graph=True the `steps` launches are captured once into a CUDA graph and the
+    graph is replayed (once untimed, once timed), so host launch overhead does not
+    leak into the measurement; every step is still one launch of the GEMM kernel.
+    """
     import torch
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                runner.launch(i)
+        with torch.cuda.stream(stream):
+            g.replay()
+            start.record(stream)
+            g.replay()
+            end.record(stream)
+        end.synchronize()
+        return start.elapsed_time(end)
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(steps):
@@ -308,10 +325,10 @@ def gpu_arm(args):
         # extra untimed warm-up so the clocks settle and the sampler sees load
         t0 = time.perf_counter()
         while not args.quick and time.perf_counter() - t0 < 1.0:
-            time_steps(runner, 20, stream)
+            time_steps(runner, 20, stream, graph=False)
         barrier()
         torch.cuda.synchronize()
-        ms_total = time_steps(runner, args.steps, stream)
+        ms_total = time_steps(runner, args.steps, stream, graph=not args.no_graph)
         torch.cuda.synchronize()
         barrier()
     ms = reduce_max(ms_total / args.steps, world, dev)
@@ -342,6 +359,7 @@ def gpu_arm(args):
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
+        "timing": "CUDA-graph replay of the K launches" if not args.no_graph else "back-to-back launches",
     }
     if rank == 0 and world == 1 and not args.no_extras:
         extras = {}
@@ -353,7 +371,7 @@ def gpu_arm(args):
                 r.launch(i, stream)
             torch.cuda.synchronize()
             n = 30 if ww.flops > 1e10 else 200
-            mse = time_steps(r, n, stream) / n
+            mse = time_steps(r, n, stream, graph=not args.no_graph) / n
             extras[name] = {"ms": round(mse, 5), "tflops": round(ww.flops / (mse * 1e-3) / 1e12, 2),
                             "roofline": roofline(ww, mse, peaks, peak_src)}
             del r
@@ -427,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time plain back-to-back launches instead of a CUDA-graph replay")
     ap.add_argument("--quick", action="store_true",
                     help="profiling mode: only W warm-up and K timed launches, short JSON line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of cpu_baseline")

@@ -56,7 +56,26 @@ bool c_d_ok(const void* C, const void* D, uint64_t bytes) {
 }  // namespace
 
 bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
-                   uint64_t pitch, uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+                   uint64_t pitch, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes) {
+    // Small per-thread cache: repeated calls on the same buffers skip the driver call.
+    struct Entry {
+        const void* base;
+        uint64_t inner, rows, pitch;
+        uint32_t box_inner, box_rows;
+        int dtype, swz;
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 16;
+    thread_local Entry cache[kEntries];
+    thread_local int cache_used = 0, cache_next = 0;
+    for (int i = 0; i < cache_used; ++i) {
+        const Entry& e = cache[i];
+        if (e.base == base && e.inner == inner && e.rows == rows && e.pitch == pitch && e.box_inner == box_inner &&
+            e.box_rows == box_rows && e.dtype == static_cast<int>(dtype) && e.swz == swizzle_bytes) {
+            *map = e.map;
+            return true;
+        }
+    }
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (enc == nullptr) return false;
     std::memset(map, 0, sizeof(*map));
@@ -64,11 +83,18 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
     const cuuint64_t strides[1] = {pitch};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t elem_strides[2] = {1, 1};
+    const CUtensorMapSwizzle swz = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    Entry& e = cache[cache_next];
+    e = Entry{base, inner, rows, pitch, box_inner, box_rows, static_cast<int>(dtype), swizzle_bytes, *map};
+    cache_next = (cache_next + 1) % kEntries;
+    if (cache_used < kEntries) ++cache_used;
+    return true;
 }
 
 }  // namespace tn

@@ -7,10 +7,11 @@
 
 namespace tn {
 
-// NVFP4: 128 x 256 tiles, one TMEM accumulator (the scale slots use the rest).
-using CfgNvfp4 = Config<KIND_NVFP4, 256, 4, 1>;
+// NVFP4: 128 x 256 tiles, one TMEM accumulator (the scale slots use the rest),
+// epilogue staged in 32 x 32 chunks (64-byte rows), single-buffered.
+using CfgNvfp4 = Config<KIND_NVFP4, 256, 4, 1, 32, 1>;
 // MXFP8: 128 x 128 tiles, double-buffered accumulator.
-using CfgMxfp8 = Config<KIND_MXFP8, 128, 6, 2>;
+using CfgMxfp8 = Config<KIND_MXFP8, 128, 6, 2, 32, 1>;
 
 static __device__ unsigned int g_err_bs;
 
@@ -45,13 +46,16 @@ gemm_status_t run(int bit, int64_t M, int64_t N, int64_t K, const void* A, const
     constexpr bool fp4 = Cfg::KIND == KIND_NVFP4;
     const int64_t row_bytes = fp4 ? K / 2 : K;    // data bytes per row
     const int64_t sf_cols = K / (fp4 ? 16 : 32);  // scale bytes per row
-    CUtensorMap ta, tb, tsa, tsb;
+    CUtensorMap ta, tb, tsa, tsb, td;
     // Data boxes: 128 bytes of K (256 E2M1 / 128 E4M3 elements) x rows, 128B swizzle.
     // Scale boxes: 16 bytes (16 scale blocks) x rows, no swizzle.
-    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, M, row_bytes, 128, Cfg::BM, true) ||
-        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, N, row_bytes, 128, Cfg::BN, true) ||
-        !encode_tma_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, sf_cols, M, sf_cols, 16, Cfg::BM, false) ||
-        !encode_tma_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, sf_cols, N, sf_cols, 16, Cfg::BN, false))
+    // D: bf16 [M][N], stored in 32-row x EPI_COLS boxes from the epilogue staging.
+    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, M, row_bytes, 128, Cfg::BM, 128) ||
+        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, N, row_bytes, 128, Cfg::BN, 128) ||
+        !encode_tma_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, sf_cols, M, sf_cols, 16, Cfg::BM, 0) ||
+        !encode_tma_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, sf_cols, N, sf_cols, 16, Cfg::BN, 0) ||
+        !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
+                       Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;
     if (ensure_attr<Cfg>(dev, bit) != cudaSuccess) return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
@@ -68,7 +72,7 @@ gemm_status_t run(int bit, int64_t M, int64_t N, int64_t K, const void* A, const
     p.err = err;
     const int tiles = p.num_m_blocks * p.num_n_blocks;
     const int grid = tiles < sms ? tiles : sms;
-    tn_gemm_kernel<Cfg><<<grid, 256, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, p);
+    tn_gemm_kernel<Cfg><<<grid, 256, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

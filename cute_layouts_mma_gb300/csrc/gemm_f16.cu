@@ -6,8 +6,10 @@
 
 namespace tn {
 
-using CfgF16Acc32 = Config<KIND_F16_ACC32, 256, 4, 2>;
-using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2>;
+// 128 x 256 tiles, 4 stages of 64 K, two TMEM accumulators, epilogue staged in
+// 32 x 64 chunks (128-byte rows), double-buffered.
+using CfgF16Acc32 = Config<KIND_F16_ACC32, 256, 4, 2, 64, 2>;
+using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2>;
 
 // Device-side record of an abandoned launch (a bounded wait ran out).
 static __device__ unsigned int g_err_f16;
@@ -40,10 +42,13 @@ unsigned int* err_word(int dev) {
 template <class Cfg>
 gemm_status_t run(int bit, int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                   void* D, cudaStream_t stream, int sms, int dev) {
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     // A: fp16 [M][K]; B: fp16 [N][K]; boxes of 64 elements (128 bytes) of K.
-    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, 64, Cfg::BM, true) ||
-        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, 64, Cfg::BN, true))
+    // D: fp16 [M][N], stored in 32-row x EPI_COLS boxes from the epilogue staging.
+    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, 64, Cfg::BM, 128) ||
+        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, 64, Cfg::BN, 128) ||
+        !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
+                       Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;
     if (ensure_attr<Cfg>(dev, bit) != cudaSuccess) return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
@@ -60,7 +65,7 @@ gemm_status_t run(int bit, int64_t M, int64_t N, int64_t K, const void* A, const
     p.err = err;
     const int tiles = p.num_m_blocks * p.num_n_blocks;
     const int grid = tiles < sms ? tiles : sms;
-    tn_gemm_kernel<Cfg><<<grid, 256, Cfg::SMEM_BYTES, stream>>>(ta, tb, ta, tb, p);
+    tn_gemm_kernel<Cfg><<<grid, 256, Cfg::SMEM_BYTES, stream>>>(ta, tb, ta, tb, td, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

@@ -18,8 +18,10 @@
 //                TCol = m // 32, byte = sfk), then signals `sf_ready`.
 //   warps 4-7    epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //                32*(w%4) .. +31, i.e. rows of the tile), adds C in fp32, rounds
-//                once to fp16 / bf16 and stores 16-byte vectors; then releases
-//                the accumulator buffer (`tmem_empty`).
+//                once to fp16 / bf16, writes the 32-row chunk to a swizzled
+//                shared-memory staging buffer and TMA-stores it (the store clips
+//                rows / columns outside D); then releases the accumulator
+//                buffer (`tmem_empty`).
 // Every wait is bounded: past the limit the kernel records a timeout in the
 // device error word, makes the other warps give up, drains its in-flight copies
 // and MMAs, frees TMEM and returns.
@@ -47,13 +49,21 @@ struct Params {
     unsigned int* err;
 };
 
-template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_>
+template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;
+    // Epilogue staging: each epilogue warp stages 32 rows x EPI_COLS outputs
+    // (64 or 128 bytes per row, 64B / 128B swizzle), EPI_BUFS buffers deep.
+    static constexpr int EPI_COLS = EPI_COLS_;
+    static constexpr int EPI_BUFS = EPI_BUFS_;
+    static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
+    static_assert(EPI_COLS == 32 || EPI_COLS == 64, "staging rows of 64 or 128 bytes");
+    static_assert(BN % EPI_COLS == 0, "whole staging chunks per tile");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
     static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
@@ -70,7 +80,8 @@ struct Config {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;  // 1024-byte aligned
+    static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUFS * EPI_BUF_BYTES;
     // barriers: full[S], empty[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = STAGES;
@@ -98,6 +109,7 @@ struct Config {
     static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per CTA");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
     static_assert(B_BYTES % 1024 == 0, "B stages stay 1024-byte aligned");
+    static_assert(OFF_EPI % 1024 == 0, "staging buffers start on a swizzle-atom boundary");
 };
 
 // Output tile -> (m block, n block), grouping 8 m blocks so that concurrently
@@ -184,29 +196,30 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One thread's 32 consecutive accumulator columns of one output row:
-// D[row][n .. n+31] = round(acc + C).  N is a multiple of 8.
-template <int KIND>
-__device__ __forceinline__ void store_chunk(const Params& p, int row, int n, const uint32_t (&r)[32]) {
-    if (row >= p.M || n >= p.N) return;
-    const int nvec = min(4, (p.N - n) >> 3);
-    const size_t off = static_cast<size_t>(row) * static_cast<size_t>(p.N) + n;
-    const uint16_t* crow = static_cast<const uint16_t*>(p.C) + off;
-    uint16_t* drow = static_cast<uint16_t*>(p.D) + off;
+// One thread's share of an epilogue chunk: output row `row`, columns n .. n+COLS-1
+// of the tile, accumulator words r[0..COLS-1].  Adds C (read directly, only for
+// in-bounds rows / 8-column groups), rounds once, and writes the packed outputs to
+// row `lane` of the warp's staging buffer in the swizzled order the D tensor map
+// uses (16-byte chunk j of row l at chunk j ^ f(l)).
+template <int KIND, int COLS>
+__device__ __forceinline__ void stage_chunk(const Params& p, int row, int n, const uint32_t* r, uint8_t* buf,
+                                            int lane) {
+    constexpr int VECS = COLS / 8;  // 16-byte output vectors per row
+    const bool has_c = p.C != nullptr && row < p.M;
+    const uint16_t* crow = static_cast<const uint16_t*>(p.C) + static_cast<size_t>(row) * p.N + n;
+    const int swz = (COLS == 64) ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        if (v < nvec) {
-            float f[8];
+    for (int v = 0; v < VECS; ++v) {
+        float f[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
-            if (p.C != nullptr) {
-                float c[8];
-                unpack8<KIND>(*reinterpret_cast<const uint4*>(crow + 8 * v), c);
+        for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
+        if (has_c && n + 8 * v < p.N) {
+            float c[8];
+            unpack8<KIND>(*reinterpret_cast<const uint4*>(crow + 8 * v), c);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] += c[i];
-            }
-            *reinterpret_cast<uint4*>(drow + 8 * v) = pack8<KIND>(f);
+            for (int i = 0; i < 8; ++i) f[i] += c[i];
         }
+        *reinterpret_cast<uint4*>(buf + lane * (COLS * 2) + ((v ^ swz) * 16)) = pack8<KIND>(f);
     }
 }
 
@@ -256,7 +269,7 @@ template <class Cfg>
 __global__ void __launch_bounds__(256, 1)
     tn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tmD, const Params p) {
     constexpr int KIND = Cfg::KIND;
     constexpr int BN = Cfg::BN;
     constexpr int STAGES = Cfg::STAGES;
@@ -290,6 +303,7 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmD);
         if constexpr (kBS) {
             tma_prefetch_desc(&tmSFA);
             tma_prefetch_desc(&tmSFB);
@@ -363,79 +377,90 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------------------------------------------------- MMA issuer
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            int t_local = 0;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t_local) {
-                const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
-                const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
-                if (!wait_bar(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
-                    ok = false;
-                    break;
+            // The CTA's (tile, k-block) pairs form one sequence of stages g.  Block-scaled:
+            // stage g+1's data is awaited and its scale tiles copied into TMEM before the
+            // MMAs of stage g are issued, so no MMA waits behind a just-issued copy.
+            constexpr bool kLookahead = kBS;
+            const int my_tiles =
+                static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
+            const int total = my_tiles * nkb;
+            auto prepare = [&](int g) -> bool {
+                const int s = g % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(g / STAGES) & 1u;
+                if (!wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) return false;
+                if constexpr (kBS) {
+                    if (!wait_bar(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) return false;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
+                if constexpr (kBS) {
+                    const uint32_t sfa_smem = sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
+                    const uint32_t sfb_smem = sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
+                    const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
+                    constexpr int SETS = (KIND == KIND_NVFP4) ? 4 : 1;  // copy sets per stage
+#pragma unroll
+                    for (int j = 0; j < SETS; ++j) {
+                        const uint32_t t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
+                        tmem_cp_32x128b_warpx4(t, smem_desc_sf_tile(sfa_smem + j * 512));
+#pragma unroll
+                        for (int h = 0; h < Cfg::SFB_GROUPS; ++h)
+                            tmem_cp_32x128b_warpx4(t + 4 + 4 * h,
+                                                   smem_desc_sf_tile(sfb_smem + (j * Cfg::SFB_GROUPS + h) * 512));
+                    }
+                }
+                return true;
+            };
+            bool ok = true;
+            if (kLookahead && total > 0) ok = prepare(0);
+            for (int g = 0; g < total && ok; ++g) {
+                const int s = g % STAGES;
+                const int t_local = g / nkb;
+                const int kb = g - t_local * nkb;
+                const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
+                const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
+                if (kb == 0) {
+                    if (!wait_bar(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    if constexpr (kBS) {
-                        if (!wait_bar(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                    }
                     tc_fence_after_sync();
-                    const uint64_t adesc = smem_desc_sw128(sbase + Cfg::OFF_A + s * Cfg::A_BYTES);
-                    const uint64_t bdesc = smem_desc_sw128(sbase + Cfg::OFF_B + s * Cfg::B_BYTES);
-                    if constexpr (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) {
-                        constexpr uint32_t idesc = idesc_f16(128, BN, KIND == KIND_F16_ACC32);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
-                    } else {
-                        const uint32_t sfa_smem = sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
-                        const uint32_t sfb_smem = sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
-                        const uint32_t sf_tmem =
-                            tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
-                        if constexpr (KIND == KIND_NVFP4) {
-                            constexpr uint32_t idesc = idesc_block_scaled(128, BN, 1u, false, 0u);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint32_t sfa_t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
-                                const uint32_t sfb_t = sfa_t + 4;
-                                tmem_cp_32x128b_warpx4(sfa_t, smem_desc_sf_tile(sfa_smem + j * 512));
-#pragma unroll
-                                for (int h = 0; h < Cfg::SFB_GROUPS; ++h)
-                                    tmem_cp_32x128b_warpx4(
-                                        sfb_t + 4 * h, smem_desc_sf_tile(sfb_smem + (j * Cfg::SFB_GROUPS + h) * 512));
-                                mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t, sfb_t,
-                                                (kb | j) != 0);
-                            }
-                        } else {
-                            const uint32_t sfa_t = sf_tmem;
-                            const uint32_t sfb_t = sf_tmem + 4;
-                            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_sf_tile(sfa_smem));
-#pragma unroll
-                            for (int h = 0; h < Cfg::SFB_GROUPS; ++h)
-                                tmem_cp_32x128b_warpx4(sfb_t + 4 * h, smem_desc_sf_tile(sfb_smem + h * 512));
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j,
-                                                idesc_block_scaled(128, BN, 0u, true, static_cast<uint32_t>(j)),
-                                                sfa_t, sfb_t, (kb | j) != 0);
-                        }
+                }
+                if (!kLookahead) {
+                    if (!prepare(g)) {
+                        ok = false;
+                        break;
                     }
-                    tc_commit(bar(Cfg::BAR_EMPTY + s));
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                } else if (g + 1 < total) {
+                    if (!prepare(g + 1)) {
+                        ok = false;
+                        break;
                     }
                 }
-                if (!ok) break;
-                tc_commit(bar(Cfg::BAR_TFULL + buf));
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const uint64_t adesc = smem_desc_sw128(sbase + Cfg::OFF_A + s * Cfg::A_BYTES);
+                const uint64_t bdesc = smem_desc_sw128(sbase + Cfg::OFF_B + s * Cfg::B_BYTES);
+                if constexpr (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) {
+                    constexpr uint32_t idesc = idesc_f16(128, BN, KIND == KIND_F16_ACC32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                } else {
+                    const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
+                    if constexpr (KIND == KIND_NVFP4) {
+                        constexpr uint32_t idesc = idesc_block_scaled(128, BN, 1u, false, 0u);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
+                            mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, (kb | j) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j,
+                                            idesc_block_scaled(128, BN, 0u, true, static_cast<uint32_t>(j)), sf_tmem,
+                                            sf_tmem + 4, (kb | j) != 0);
+                    }
+                }
+                tc_commit(bar(Cfg::BAR_EMPTY + s));
+                if (kb == nkb - 1) tc_commit(bar(Cfg::BAR_TFULL + buf));
             }
             if (!ok) {
                 // Abandoning: wait for the MMAs and copies already issued.
@@ -474,7 +499,11 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else if (warp >= 4) {
         // -------------------------------------------------------------- epilogue
+        constexpr int EC = Cfg::EPI_COLS;
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint8_t* stg = smem + Cfg::OFF_EPI + q * (Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+        const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + q * (Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+        int eb = 0;
         int t_local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_local) {
             const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
@@ -485,20 +514,35 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after_sync();
             int mb, nb;
             tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
-            const int row = mb * Cfg::BM + q * 32 + lane;
+            const int m_warp = mb * Cfg::BM + q * 32;  // first output row of this warp
             const int n0 = nb * BN;
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < BN; c += EC) {
                 if (n0 + c >= p.N) break;  // warp-uniform
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), r);
+                uint32_t r[EC];
+                tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                if constexpr (EC == 64)
+                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
-                store_chunk<KIND>(p, row, n0 + c, r);
+                if (m_warp >= p.M) continue;  // no row of this warp lies inside D
+                // the staging buffer is free once the store issued from it has read it
+                if (lane == 0) bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
+                __syncwarp();
+                stage_chunk<KIND, EC>(p, m_warp + lane, n0 + c, r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmD, stg_u32 + eb * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
+                    bulk_commit_group();
+                }
+                if constexpr (Cfg::EPI_BUFS == 2) eb ^= 1;
             }
             tc_fence_before_sync();
             mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
         }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before_sync();

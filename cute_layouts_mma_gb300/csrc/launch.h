@@ -12,11 +12,12 @@ namespace tn {
 
 // Encode a 2-D tiled TMA map over a row-major matrix: `inner` elements per row
 // (contiguous), `rows` rows `pitch` bytes apart, boxes of box_inner x box_rows.
-// swizzle128: 128-byte XOR swizzle in shared memory (box rows of 128 bytes).
+// swizzle_bytes: 0 (none), 64 or 128 -- the XOR swizzle of the box in shared
+// memory (box rows of at most that many bytes).  Maps are cached per thread.
 // Returns false if the driver rejects the map.
 bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t pitch, uint32_t box_inner, uint32_t box_rows,
-                   bool swizzle128);
+                   int swizzle_bytes);
 
 // Launchers; arguments are already validated.  `sms` is the SM count of the
 // current device, `dev` its ordinal.
