@@ -72,7 +72,7 @@ gemm_status_t run(int bit, int64_t M, int64_t N, int64_t K, const void* A, const
     p.err = err;
     const int tiles = p.num_m_blocks * p.num_n_blocks;
     const int grid = tiles < sms ? tiles : sms;
-    tn_gemm_kernel<Cfg><<<grid, 256, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
+    tn_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, td, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

@@ -10,12 +10,13 @@
 //   warp 1       MMA issuer (one thread): tcgen05.mma into a TMEM accumulator,
 //                four K steps per stage; tcgen05.commit frees the stage
 //                (`empty`) and, at the end of a tile, hands the accumulator to the
-//                epilogue (`tmem_full`).  Block-scaled: first tcgen05.cp of the
-//                packed scale tiles into TMEM.
-//   warp 2       (block-scaled only) scale-factor packer: rewrites each stage's
-//                row-major scale box, in place, into the 32-lane x 16-byte base
-//                tiles that tcgen05.cp ... .warpx4 copies (local_lane = m % 32,
-//                TCol = m // 32, byte = sfk), then signals `sf_ready`.
+//                epilogue (`tmem_full`).
+//   warps 8-11   (block-scaled only) scale writers, one per TMEM lane quarter:
+//                each turns the stage's row-major scale boxes into the 32-lane
+//                base tiles the block-scaled MMA reads (local_lane = m % 32,
+//                TCol = m // 32, byte = sfk) and writes them with tcgen05.st into
+//                its own 32 lanes -- the four quarters together replicate the
+//                tile to all four lane partitions -- then signals `sf_ready`.
 //   warps 4-7    epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //                32*(w%4) .. +31, i.e. rows of the tile), adds C in fp32, rounds
 //                once to fp16 / bf16, writes the 32-row chunk to a swizzled
@@ -65,6 +66,8 @@ struct Config {
     static_assert(EPI_COLS == 32 || EPI_COLS == 64, "staging rows of 64 or 128 bytes");
     static_assert(BN % EPI_COLS == 0, "whole staging chunks per tile");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
+    // warps 0-7 (producer, MMA, idle x2, epilogue x4), plus 4 scale writers
+    static constexpr int THREADS = kBlockScaled ? 384 : 256;
     static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
     static constexpr int kKCoordPerStage = (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) ? 64 : 128;
@@ -95,7 +98,7 @@ struct Config {
 
     // TMEM: ACC_BUFS accumulators of BN fp32 columns, then the scale-factor slots.
     static constexpr int SF_COL0 = ACC_BUFS * BN;
-    static constexpr int SF_COLS_PER_COPYSET = 4 * (1 + SFB_GROUPS);  // SFA tile + SFB tiles
+    static constexpr int SF_COLS_PER_COPYSET = 4 * (1 + SFB_GROUPS);  // SFA tile + SFB tiles (one MMA)
     static constexpr int SF_COLS_PER_STAGE =
         KIND == KIND_NVFP4 ? kMmasPerStage * SF_COLS_PER_COPYSET
                            : (KIND == KIND_MXFP8 ? SF_COLS_PER_COPYSET : 0);
@@ -110,6 +113,7 @@ struct Config {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
     static_assert(B_BYTES % 1024 == 0, "B stages stay 1024-byte aligned");
     static_assert(OFF_EPI % 1024 == 0, "staging buffers start on a swizzle-atom boundary");
+    static_assert(KIND != KIND_MXFP8 || SFB_GROUPS == 1, "MXFP8 scale writer handles one 128-row B group");
 };
 
 // Output tile -> (m block, n block), grouping 8 m blocks so that concurrently
@@ -223,50 +227,55 @@ __device__ __forceinline__ void stage_chunk(const Params& p, int row, int n, con
     }
 }
 
-// In-place repack of one stage's raw scale box (row r of the box at bytes
-// 16r .. 16r+15, holding sfk = 16c .. 16c+15 for this K range) into the base
-// tiles tcgen05.cp reads: tile (j, h) = scales 4j..4j+3 of rows 128h .. 128h+127,
-// 32 local lanes x 16 bytes, lane l holding rows 128h + l + 32*Mgroup for
-// Mgroup = 0..3 at bytes 4*Mgroup .. 4*Mgroup+3 ("数据布局及其记号": local_lane =
-// m % 32, TCol = m // 32, byte = sfk).  NVFP4: all four words of the box feed
-// the stage's four MMAs, tiles ordered (j, h).  MXFP8: only word `w` (this
-// stage's four scales) is used; one tile per 128-row group.
-template <int GROUPS, bool kAllWords>
-__device__ __forceinline__ void repack_scales(uint8_t* buf, int lane, int w) {
-    uint4* v4 = reinterpret_cast<uint4*>(buf);
-    if constexpr (kAllWords) {
-        uint32_t R[GROUPS][4][4];
+// Scale-factor writer for one TMEM lane quarter.  The stage's scale boxes sit in
+// shared memory row-major: row r of a box at bytes 16r .. 16r+15 holds scale
+// blocks sfk = 16c .. 16c+15 of that row.  Lane l of the warp (TMEM lane
+// 32q + l) receives, for each copy set j, the base-tile row l: SFA scales of rows
+// l, l+32, l+64, l+96 in columns 0..3 (TCol = m // 32, the four scales of the
+// MMA in bytes 0..3, byte = sfk), then the SFB scales of rows l + 32c in
+// columns 4 + c ("数据布局及其记号", block-scaled section).  NVFP4 has one copy
+// set per MMA (word j of each row = that MMA's 4 scales); MXFP8 has one copy set
+// per stage (word `word` of each row = the stage's 4 scales, one per MMA, picked
+// by the MMA's scale-factor ID).  Every quarter writes the same values: together
+// the four warps replicate the tile to the four lane partitions.
+template <int KIND, int GROUPS>
+__device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t* raw_b, int lane, int word,
+                                             uint32_t taddr) {
+    constexpr int SET = 4 + 4 * GROUPS;
+    if constexpr (KIND == KIND_NVFP4) {
+        uint32_t R[SET][4];
 #pragma unroll
-        for (int h = 0; h < GROUPS; ++h)
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint4 x = v4[h * 128 + 32 * g + lane];
-                R[h][g][0] = x.x;
-                R[h][g][1] = x.y;
-                R[h][g][2] = x.z;
-                R[h][g][3] = x.w;
-            }
-        __syncwarp();
+        for (int c = 0; c < SET; ++c) {
+            const uint8_t* src = (c < 4) ? raw_a + (lane + 32 * c) * 16 : raw_b + (lane + 32 * (c - 4)) * 16;
+            const uint4 x = *reinterpret_cast<const uint4*>(src);
+            R[c][0] = x.x;
+            R[c][1] = x.y;
+            R[c][2] = x.z;
+            R[c][3] = x.w;
+        }
+        uint32_t out[4 * SET];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int h = 0; h < GROUPS; ++h)
-                v4[(j * GROUPS + h) * 32 + lane] = make_uint4(R[h][0][j], R[h][1][j], R[h][2][j], R[h][3][j]);
+            for (int c = 0; c < SET; ++c) out[j * SET + c] = R[c][j];
+        static_assert((4 * SET) % 16 == 0, "whole 16-column stores");
+#pragma unroll
+        for (int i = 0; i < (4 * SET) / 16; ++i)
+            tmem_st_32x32b_x16(taddr + 16 * i, *reinterpret_cast<const uint32_t(*)[16]>(&out[16 * i]));
     } else {
-        const uint32_t* v1 = reinterpret_cast<const uint32_t*>(buf);
-        uint32_t R[GROUPS][4];
+        static_assert(SET == 8, "one SFA tile and one SFB tile per stage");
+        uint32_t out[SET];
 #pragma unroll
-        for (int h = 0; h < GROUPS; ++h)
-#pragma unroll
-            for (int g = 0; g < 4; ++g) R[h][g] = v1[(h * 128 + 32 * g + lane) * 4 + w];
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < GROUPS; ++h) v4[h * 32 + lane] = make_uint4(R[h][0], R[h][1], R[h][2], R[h][3]);
+        for (int c = 0; c < SET; ++c) {
+            const uint8_t* src = (c < 4) ? raw_a + (lane + 32 * c) * 16 : raw_b + (lane + 32 * (c - 4)) * 16;
+            out[c] = reinterpret_cast<const uint32_t*>(src)[word];
+        }
+        tmem_st_32x32b_x8(taddr, out);
     }
 }
 
 template <class Cfg>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
     tn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                    const __grid_constant__ CUtensorMap tmD, const Params p) {
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(Cfg::BAR_FULL + s), 1);
             mbar_init(bar(Cfg::BAR_EMPTY + s), 1);
-            mbar_init(bar(Cfg::BAR_SF + s), 1);
+            mbar_init(bar(Cfg::BAR_SF + s), 4);  // one arrival per scale-writer warp
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(bar(Cfg::BAR_TFULL + b), 1);
@@ -377,42 +386,14 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------------------------------------------------- MMA issuer
-            // The CTA's (tile, k-block) pairs form one sequence of stages g.  Block-scaled:
-            // stage g+1's data is awaited and its scale tiles copied into TMEM before the
-            // MMAs of stage g are issued, so no MMA waits behind a just-issued copy.
-            constexpr bool kLookahead = kBS;
+            // The CTA's (tile, k-block) pairs form one sequence of stages g.
             const int my_tiles =
                 static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
             const int total = my_tiles * nkb;
-            auto prepare = [&](int g) -> bool {
-                const int s = g % STAGES;
-                const uint32_t ph = static_cast<uint32_t>(g / STAGES) & 1u;
-                if (!wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) return false;
-                if constexpr (kBS) {
-                    if (!wait_bar(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) return false;
-                }
-                tc_fence_after_sync();
-                if constexpr (kBS) {
-                    const uint32_t sfa_smem = sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
-                    const uint32_t sfb_smem = sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
-                    const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
-                    constexpr int SETS = (KIND == KIND_NVFP4) ? 4 : 1;  // copy sets per stage
-#pragma unroll
-                    for (int j = 0; j < SETS; ++j) {
-                        const uint32_t t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
-                        tmem_cp_32x128b_warpx4(t, smem_desc_sf_tile(sfa_smem + j * 512));
-#pragma unroll
-                        for (int h = 0; h < Cfg::SFB_GROUPS; ++h)
-                            tmem_cp_32x128b_warpx4(t + 4 + 4 * h,
-                                                   smem_desc_sf_tile(sfb_smem + (j * Cfg::SFB_GROUPS + h) * 512));
-                    }
-                }
-                return true;
-            };
             bool ok = true;
-            if (kLookahead && total > 0) ok = prepare(0);
             for (int g = 0; g < total && ok; ++g) {
                 const int s = g % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(g / STAGES) & 1u;
                 const int t_local = g / nkb;
                 const int kb = g - t_local * nkb;
                 const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
@@ -422,19 +403,18 @@ __global__ void __launch_bounds__(256, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();
                 }
-                if (!kLookahead) {
-                    if (!prepare(g)) {
-                        ok = false;
-                        break;
-                    }
-                } else if (g + 1 < total) {
-                    if (!prepare(g + 1)) {
+                if (!wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                if constexpr (kBS) {
+                    if (!wait_bar(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                 }
+                tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 const uint64_t adesc = smem_desc_sw128(sbase + Cfg::OFF_A + s * Cfg::A_BYTES);
                 const uint64_t bdesc = smem_desc_sw128(sbase + Cfg::OFF_B + s * Cfg::B_BYTES);
@@ -468,9 +448,11 @@ __global__ void __launch_bounds__(256, 1)
                 wait_bar_drain(bar(Cfg::BAR_DRAIN), 0u);
             }
         }
-    } else if (warp == 2) {
+    } else if (warp >= 8) {
         if constexpr (kBS) {
-            // -------------------------------------------------------------- scale packer
+            // -------------------------------------------------------------- scale writers
+            const int q = warp & 3;  // TMEM lane quarter this warp may access
+            const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -478,16 +460,11 @@ __global__ void __launch_bounds__(256, 1)
                 for (int kb = 0; kb < nkb; ++kb) {
                     ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err));
                     if (!ok) break;
-                    uint8_t* sfa = smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES;
-                    uint8_t* sfb = smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES;
-                    if constexpr (KIND == KIND_NVFP4) {
-                        repack_scales<1, true>(sfa, lane, 0);
-                        repack_scales<Cfg::SFB_GROUPS, true>(sfb, lane, 0);
-                    } else {
-                        repack_scales<1, false>(sfa, lane, kb & 3);
-                        repack_scales<Cfg::SFB_GROUPS, false>(sfb, lane, kb & 3);
-                    }
-                    fence_proxy_async_smem();
+                    write_scales<KIND, Cfg::SFB_GROUPS>(
+                        smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, lane,
+                        kb & 3, lane_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE));
+                    tmem_st_wait();
+                    tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(Cfg::BAR_SF + s));
                     if (++s == STAGES) {
