@@ -3,26 +3,40 @@
 // FP16 or in the block-scaled NVFP4 / MXFP8 forms ("数据布局及其记号", block-scaled
 // MMA section).
 //
-// One CTA per SM walks output tiles of 128 x BN.  Its warps:
-//   warp 0       TMA producer: per 128-byte K slice, loads the A and B boxes into
-//                128B-swizzled shared memory (and, block-scaled, the raw scale
-//                boxes), arming the stage's `full` barrier with the byte count.
-//   warp 1       MMA issuer (one thread): tcgen05.mma into a TMEM accumulator,
-//                four K steps per stage; tcgen05.commit frees the stage
-//                (`empty`) and, at the end of a tile, hands the accumulator to the
-//                epilogue (`tmem_full`).
+// Output tiles are (128 * PAIR) x BN.  With PAIR = 2 the two CTAs of a (2,1,1)
+// cluster share a tile: CTA r loads A rows 128r .. 128r+127 and B rows
+// (BN/2)r .. (BN/2)(r+1)-1 of the tile into its own shared memory, the leader
+// (r = 0) issues one cta_group::2 MMA of 256 x BN per K step over both CTAs'
+// operands, and each CTA's TMEM accumulates its own 128 rows x BN.  Per SM this
+// halves the B bytes loaded from L2 and read by the tensor core.
+//
+// Warps of each CTA:
+//   warps 0, 2   TMA issuers for A and B: per 128-byte K slice, load this CTA's A
+//                (warp 0) and B (warp 2) box into 128B-swizzled shared memory and
+//                arm the leader's `full` barrier with the bytes (PAIR = 2: the
+//                peer's copies signal the leader's barrier directly).  A TMA
+//                instruction occupies its issuing warp for a few hundred cycles
+//                whatever the box size, so each operand stream has its own warp.
+//   warps 3, 12  (block-scaled only) TMA issuers of the raw scale boxes (this
+//                CTA's 128 SFA rows, all BN SFB rows of the tile) on `sf_full`.
+//   warp 1       TMEM allocation; in the leader, the MMA issuer (one thread):
+//                tcgen05.mma into a TMEM accumulator, four K steps per stage;
+//                tcgen05.commit frees the stage (`empty`, in both CTAs) and, at the
+//                end of a tile, hands the accumulator to the epilogues
+//                (`tmem_full`, in both CTAs).
+//   warps 4-7    epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//                32*(w%4) .. +31, i.e. rows of the tile), adds C in fp32, rounds
+//                once to fp16 / bf16, writes the 32-row chunk to a swizzled
+//                shared-memory staging buffer and TMA-stores it (the store clips
+//                rows / columns outside D); then releases the accumulator on the
+//                leader's `tmem_empty`.
 //   warps 8-11   (block-scaled only) scale writers, one per TMEM lane quarter:
 //                each turns the stage's row-major scale boxes into the 32-lane
 //                base tiles the block-scaled MMA reads (local_lane = m % 32,
 //                TCol = m // 32, byte = sfk) and writes them with tcgen05.st into
 //                its own 32 lanes -- the four quarters together replicate the
-//                tile to all four lane partitions -- then signals `sf_ready`.
-//   warps 4-7    epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//                32*(w%4) .. +31, i.e. rows of the tile), adds C in fp32, rounds
-//                once to fp16 / bf16, writes the 32-row chunk to a swizzled
-//                shared-memory staging buffer and TMA-stores it (the store clips
-//                rows / columns outside D); then releases the accumulator
-//                buffer (`tmem_empty`).
+//                tile to all four lane partitions -- then arrive on the leader's
+//                `sf_ready`.
 // Every wait is bounded: past the limit the kernel records a timeout in the
 // device error word, makes the other warps give up, drains its in-flight copies
 // and MMAs, frees TMEM and returns.
@@ -50,11 +64,14 @@ struct Params {
     unsigned int* err;
 };
 
-template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_>
+template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_>
 struct Config {
     static constexpr int KIND = KIND_;
-    static constexpr int BM = 128;
-    static constexpr int BN = BN_;
+    static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
+    static constexpr int BM = 128;      // output rows per CTA
+    static constexpr int BM_TILE = BM * PAIR;
+    static constexpr int BN = BN_;      // output columns per tile (MMA N)
+    static constexpr int BN_CTA = BN / PAIR;  // B rows loaded per CTA
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;
     // Epilogue staging: each epilogue warp stages 32 rows x EPI_COLS outputs
@@ -65,19 +82,22 @@ struct Config {
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
     static_assert(EPI_COLS == 32 || EPI_COLS == 64, "staging rows of 64 or 128 bytes");
     static_assert(BN % EPI_COLS == 0, "whole staging chunks per tile");
+    static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
-    // warps 0-7 (producer, MMA, idle x2, epilogue x4), plus 4 scale writers
-    static constexpr int THREADS = kBlockScaled ? 384 : 256;
+    // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
+    // writers, 12 SFB issuer
+    static constexpr int THREADS = kBlockScaled ? 416 : 256;
     static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
     static constexpr int kKCoordPerStage = (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) ? 64 : 128;
 
     static constexpr int A_BYTES = BM * 128;
-    static constexpr int B_BYTES = BN * 128;
+    static constexpr int B_BYTES = BN_CTA * 128;
     static constexpr int SFB_GROUPS = kBlockScaled ? (BN + 127) / 128 : 0;  // 128-row scale groups
     static constexpr int SFA_BYTES = kBlockScaled ? BM * 16 : 0;
     static constexpr int SFB_BYTES = SFB_GROUPS * 128 * 16;
-    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + (kBlockScaled ? (BM + BN) * 16 : 0);
+    static constexpr uint32_t TX_BYTES = PAIR * (A_BYTES + B_BYTES);             // both CTAs' operands
+    static constexpr uint32_t SF_TX_BYTES = kBlockScaled ? (BM + BN) * 16 : 0;  // this CTA's scales
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -85,18 +105,19 @@ struct Config {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;  // 1024-byte aligned
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUFS * EPI_BUF_BYTES;
-    // barriers: full[S], empty[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain
+    // barriers: full[S], empty[S], sf_full[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = STAGES;
-    static constexpr int BAR_SF = 2 * STAGES;
-    static constexpr int BAR_TFULL = 3 * STAGES;
-    static constexpr int BAR_TEMPTY = 3 * STAGES + ACC_BUFS;
-    static constexpr int BAR_DRAIN = 3 * STAGES + 2 * ACC_BUFS;
+    static constexpr int BAR_SFFULL = 2 * STAGES;
+    static constexpr int BAR_SF = 3 * STAGES;
+    static constexpr int BAR_TFULL = 4 * STAGES;
+    static constexpr int BAR_TEMPTY = 4 * STAGES + ACC_BUFS;
+    static constexpr int BAR_DRAIN = 4 * STAGES + 2 * ACC_BUFS;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM base address, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 
-    // TMEM: ACC_BUFS accumulators of BN fp32 columns, then the scale-factor slots.
+    // TMEM (per CTA): ACC_BUFS accumulators of BN fp32 columns, then the scale slots.
     static constexpr int SF_COL0 = ACC_BUFS * BN;
     static constexpr int SF_COLS_PER_COPYSET = 4 * (1 + SFB_GROUPS);  // SFA tile + SFB tiles (one MMA)
     static constexpr int SF_COLS_PER_STAGE =
@@ -110,7 +131,7 @@ struct Config {
                                                         : 512;
     static_assert(TMEM_USED <= 512, "TMEM holds 512 columns");
     static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per CTA");
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
+    static_assert(BN % (16 * PAIR) == 0 && BN >= 16 && BN <= 256, "MMA N: multiple of 16 (32 for a pair), <= 256");
     static_assert(B_BYTES % 1024 == 0, "B stages stay 1024-byte aligned");
     static_assert(OFF_EPI % 1024 == 0, "staging buffers start on a swizzle-atom boundary");
     static_assert(KIND != KIND_MXFP8 || SFB_GROUPS == 1, "MXFP8 scale writer handles one 128-row B group");
@@ -130,13 +151,16 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
 }
 
 // Bounded parity wait.  Returns false (and stops the other warps) after the
-// time limit, or as soon as another warp has given up.
+// time limit, or as soon as another warp has given up.  kCluster: acquire at
+// cluster scope (the barrier receives arrivals from the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -153,6 +177,13 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (global_timer_ns() - t0 > kDrainLimitNs) return;
+    }
+}
+
+// Bounded pause used while abandoning work when completions cannot be observed.
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) {
     }
 }
 
@@ -280,30 +311,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                    const __grid_constant__ CUtensorMap tmD, const Params p) {
     constexpr int KIND = Cfg::KIND;
+    constexpr int PAIR = Cfg::PAIR;
     constexpr int BN = Cfg::BN;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int ACC_BUFS = Cfg::ACC_BUFS;
     constexpr bool kBS = Cfg::kBlockScaled;
+    constexpr bool kPair = PAIR == 2;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0 = leader
+    const bool leader = rank == 0;
+    const int cluster = static_cast<int>(blockIdx.x) / PAIR;
+    const int num_clusters = static_cast<int>(gridDim.x) / PAIR;
 
     auto bar = [&](int i) -> uint32_t { return sbase + Cfg::OFF_BAR + 8 * i; };
+    // the leader's copy of barrier i, as seen from this CTA
+    auto leader_bar = [&](int i) -> uint32_t { return kPair ? mapa_shared(bar(i), 0u) : bar(i); };
     volatile uint32_t* tmem_base_slot = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(Cfg::BAR_FULL + s), 1);
+            mbar_init(bar(Cfg::BAR_FULL + s), 2);    // the leader's A and B issuers
             mbar_init(bar(Cfg::BAR_EMPTY + s), 1);
-            mbar_init(bar(Cfg::BAR_SF + s), 4);  // one arrival per scale-writer warp
+            mbar_init(bar(Cfg::BAR_SFFULL + s), 2);  // SFA and SFB issuers
+            mbar_init(bar(Cfg::BAR_SF + s), 4 * PAIR);  // one arrival per scale-writer warp
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(bar(Cfg::BAR_TFULL + b), 1);
-            mbar_init(bar(Cfg::BAR_TEMPTY + b), 128);
+            mbar_init(bar(Cfg::BAR_TEMPTY + b), 4 * PAIR);  // one arrival per epilogue warp
         }
         mbar_init(bar(Cfg::BAR_DRAIN), 1);
         *abort_flag = 0;
@@ -319,56 +359,83 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc(sbase + Cfg::OFF_MISC, Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(sbase + Cfg::OFF_MISC, Cfg::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(sbase + Cfg::OFF_MISC, Cfg::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_slot;
 
     const int num_tiles = p.num_m_blocks * p.num_n_blocks;
     const int nkb = p.num_k_blocks;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------------------- producer
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t loads[STAGES];
+    // ------------------------------------------------------------------ TMA issuers
+    // role 0: A, 1: B, 2: SFA, 3: SFB.  Each waits for its stage slot to be released
+    // by the MMAs that last read it, arms its barrier with its bytes and issues one box.
+    auto issue_loop = [&](const int role) {
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t loads[STAGES];
 #pragma unroll
-            for (int i = 0; i < STAGES; ++i) loads[i] = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                int mb, nb;
-                tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
-                const int m0 = mb * Cfg::BM, n0 = nb * BN;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar(Cfg::BAR_FULL + s);
-                    mbar_arrive_expect_tx(fb, Cfg::TX_BYTES);
+        for (int i = 0; i < STAGES; ++i) loads[i] = 0;
+        bool ok = true;
+        for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
+            int mb, nb;
+            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
+            const int m0 = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM;  // this CTA's A rows
+            const int nb0 = nb * BN;                                              // tile's first column
+            const int n0 = nb0 + static_cast<int>(rank) * Cfg::BN_CTA;           // this CTA's B rows
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                if (role <= 1) {
                     const int kx = kb * Cfg::kKCoordPerStage;
-                    tma_load_2d(sbase + Cfg::OFF_A + s * Cfg::A_BYTES, &tmA, fb, kx, m0);
-                    tma_load_2d(sbase + Cfg::OFF_B + s * Cfg::B_BYTES, &tmB, fb, kx, n0);
-                    if constexpr (kBS) {
-                        // 16 scale bytes per row per box; NVFP4 uses all 16 in this stage,
-                        // MXFP8 uses 4 of them (so the same box serves 4 stages).
-                        const int sfx = (KIND == KIND_NVFP4) ? kb * 16 : (kb >> 2) * 16;
-                        tma_load_2d(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, &tmSFA, fb, sfx, m0);
-                        tma_load_2d(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, &tmSFB, fb, sfx, n0);
+                    const uint32_t dst = role == 0 ? sbase + Cfg::OFF_A + s * Cfg::A_BYTES
+                                                   : sbase + Cfg::OFF_B + s * Cfg::B_BYTES;
+                    const CUtensorMap* map = role == 0 ? &tmA : &tmB;
+                    const int y = role == 0 ? m0 : n0;
+                    const uint32_t bytes = PAIR * (role == 0 ? Cfg::A_BYTES : Cfg::B_BYTES);
+                    if constexpr (kPair) {
+                        if (leader) mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
+                        tma_load_2d_pair(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y);
+                    } else {
+                        mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
+                        tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
                     }
-                    ++loads[s];
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                } else if constexpr (kBS) {
+                    // 16 scale bytes per row per box; NVFP4 uses all 16 in this stage,
+                    // MXFP8 uses 4 of them (so the same box serves 4 stages).
+                    const int sfx = (KIND == KIND_NVFP4) ? kb * 16 : (kb >> 2) * 16;
+                    const uint32_t sb = bar(Cfg::BAR_SFFULL + s);
+                    if (role == 2) {
+                        mbar_arrive_expect_tx(sb, Cfg::BM * 16);
+                        tma_load_2d(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, &tmSFA, sb, sfx, m0);
+                    } else {
+                        mbar_arrive_expect_tx(sb, BN * 16);
+                        tma_load_2d(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, &tmSFB, sb, sfx, nb0);
                     }
                 }
+                ++loads[s];
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
-            if (ok) {
-                // Wait until the consumer has released every stage, so that no
+        }
+        if (ok) {
+            if (role == 0) {
+                // Wait until the MMAs have released every stage, so that no
                 // tcgen05.commit arrival is still in flight when the CTA exits.
                 for (int i = 0; i < STAGES; ++i) {
                     if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) break;
@@ -377,78 +444,119 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ph ^= 1u;
                     }
                 }
-            } else {
-                // Abandoning: let every issued TMA copy land before the CTA exits.
-                for (int i = 0; i < STAGES; ++i)
-                    if (loads[i] > 0) wait_bar_drain(bar(Cfg::BAR_FULL + i), (loads[i] - 1u) & 1u);
             }
+        } else {
+            // Abandoning: let every issued TMA copy land before the CTA exits.
+            for (int i = 0; i < STAGES; ++i) {
+                if (loads[i] == 0) continue;
+                if (role >= 2)
+                    wait_bar_drain(bar(Cfg::BAR_SFFULL + i), (loads[i] - 1u) & 1u);
+                else if (!kPair || leader)
+                    wait_bar_drain(bar(Cfg::BAR_FULL + i), (loads[i] - 1u) & 1u);
+            }
+            // the peer's operand copies signal the leader's barriers: give them time
+            if (kPair && role <= 1) pause_ns(kDrainLimitNs / 4);
         }
+    };
+
+    if (warp == 0 || warp == 2 || (kBS && (warp == 3 || warp == 12))) {
+        if (lane == 0) issue_loop(warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : 3);
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ---------------------------------------------------------- MMA issuer
-            // The CTA's (tile, k-block) pairs form one sequence of stages g.
-            const int my_tiles =
-                static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
-            const int total = my_tiles * nkb;
+            // One thread issues every MMA; each tcgen05 instruction costs it tens of
+            // cycles, so the loop keeps its own bookkeeping incremental (no divisions)
+            // and the shared-memory descriptors precomputed.
+            const int my_tiles = cluster < num_tiles ? (num_tiles - 1 - cluster) / num_clusters + 1 : 0;
+            constexpr uint32_t kM = 128 * PAIR;
+            // descriptor of stage 0; stage s adds s * (bytes / 16) to the start address
+            const uint64_t adesc0 = smem_desc_sw128(sbase + Cfg::OFF_A);
+            const uint64_t bdesc0 = smem_desc_sw128(sbase + Cfg::OFF_B);
             bool ok = true;
-            for (int g = 0; g < total && ok; ++g) {
-                const int s = g % STAGES;
-                const uint32_t ph = static_cast<uint32_t>(g / STAGES) & 1u;
-                const int t_local = g / nkb;
-                const int kb = g - t_local * nkb;
-                const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
-                const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
-                if (kb == 0) {
-                    if (!wait_bar(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t_local = 0; t_local < my_tiles && ok; ++t_local) {
+                const int buf = (ACC_BUFS == 1) ? 0 : (t_local & 1);
+                const uint32_t use = static_cast<uint32_t>(ACC_BUFS == 1 ? t_local : (t_local >> 1));
+                if (!wait_bar<kPair>(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                if constexpr (kBS) {
-                    if (!wait_bar(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) {
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bar<kPair>(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                const uint64_t adesc = smem_desc_sw128(sbase + Cfg::OFF_A + s * Cfg::A_BYTES);
-                const uint64_t bdesc = smem_desc_sw128(sbase + Cfg::OFF_B + s * Cfg::B_BYTES);
-                if constexpr (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) {
-                    constexpr uint32_t idesc = idesc_f16(128, BN, KIND == KIND_F16_ACC32);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
-                } else {
-                    const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
-                    if constexpr (KIND == KIND_NVFP4) {
-                        constexpr uint32_t idesc = idesc_block_scaled(128, BN, 1u, false, 0u);
+                    if constexpr (kBS) {
+                        if (!wait_bar<kPair>(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t adesc = adesc0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s * (Cfg::B_BYTES >> 4));
+                    if constexpr (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) {
+                        constexpr uint32_t idesc = idesc_f16(kM, BN, KIND == KIND_F16_ACC32);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint32_t t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
-                            mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, (kb | j) != 0);
+                            if constexpr (kPair)
+                                mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                            else
+                                mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
                         }
                     } else {
+                        const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
+                        if constexpr (KIND == KIND_NVFP4) {
+                            constexpr uint32_t idesc = idesc_block_scaled(kM, BN, 1u, false, 0u);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j,
-                                            idesc_block_scaled(128, BN, 0u, true, static_cast<uint32_t>(j)), sf_tmem,
-                                            sf_tmem + 4, (kb | j) != 0);
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
+                                if constexpr (kPair)
+                                    mma_mxf4nvf4_4x_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, (kb | j) != 0);
+                                else
+                                    mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, (kb | j) != 0);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                constexpr uint32_t idesc0 = idesc_block_scaled(kM, BN, 0u, true, 0u);
+                                const uint32_t idesc = idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+                                if constexpr (kPair)
+                                    mma_mxf8f6f4_1x_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
+                                                         (kb | j) != 0);
+                                else
+                                    mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
+                                                    (kb | j) != 0);
+                            }
+                        }
+                    }
+                    if constexpr (kPair)
+                        tc_commit_pair(bar(Cfg::BAR_EMPTY + s), 0x3);
+                    else
+                        tc_commit(bar(Cfg::BAR_EMPTY + s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
                     }
                 }
-                tc_commit(bar(Cfg::BAR_EMPTY + s));
-                if (kb == nkb - 1) tc_commit(bar(Cfg::BAR_TFULL + buf));
+                if (!ok) break;
+                if constexpr (kPair)
+                    tc_commit_pair(bar(Cfg::BAR_TFULL + buf), 0x3);
+                else
+                    tc_commit(bar(Cfg::BAR_TFULL + buf));
             }
             if (!ok) {
-                // Abandoning: wait for the MMAs and copies already issued.
-                tc_commit(bar(Cfg::BAR_DRAIN));
+                // Abandoning: wait for the MMAs already issued.
+                if constexpr (kPair)
+                    tc_commit_pair(bar(Cfg::BAR_DRAIN), 0x1);
+                else
+                    tc_commit(bar(Cfg::BAR_DRAIN));
                 wait_bar_drain(bar(Cfg::BAR_DRAIN), 0u);
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 8 && warp < 12) {
         if constexpr (kBS) {
             // -------------------------------------------------------------- scale writers
             const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -456,9 +564,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
                 for (int kb = 0; kb < nkb; ++kb) {
-                    ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err));
+                    ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_SFFULL + s), ph, abort_flag, p.err));
                     if (!ok) break;
                     write_scales<KIND, Cfg::SFB_GROUPS>(
                         smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, lane,
@@ -466,7 +574,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tmem_st_wait();
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(Cfg::BAR_SF + s));
+                    if (lane == 0) {
+                        if constexpr (kPair)
+                            mbar_arrive_cluster(leader_bar(Cfg::BAR_SF + s));
+                        else
+                            mbar_arrive(bar(Cfg::BAR_SF + s));
+                    }
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
@@ -474,7 +587,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // -------------------------------------------------------------- epilogue
         constexpr int EC = Cfg::EPI_COLS;
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -482,7 +595,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + q * (Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
         int eb = 0;
         int t_local = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_local) {
+        for (int tile = cluster; tile < num_tiles; tile += num_clusters, ++t_local) {
             const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
             const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
             const bool ok =
@@ -491,7 +604,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc_fence_after_sync();
             int mb, nb;
             tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
-            const int m_warp = mb * Cfg::BM + q * 32;  // first output row of this warp
+            // first output row of this warp
+            const int m_warp = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM + q * 32;
             const int n0 = nb * BN;
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
 #pragma unroll 1
@@ -516,18 +630,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if constexpr (Cfg::EPI_BUFS == 2) eb ^= 1;
             }
             tc_fence_before_sync();
-            mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (kPair)
+                    mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                else
+                    mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+            }
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync_all();  // no CTA leaves while its peer may still signal or read it
+    else
+        __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
