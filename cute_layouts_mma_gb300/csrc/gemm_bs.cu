@@ -6,14 +6,13 @@
 
 namespace tn {
 
-// NVFP4, CTA pairs (M > 128): 256 x 256 tiles, 5 stages, one TMEM accumulator (the
-// scale slots use the rest), epilogue staged in 32 x 32 chunks, single-buffered.
-using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 5, 1, 32, 1, 2>;
-// NVFP4, single CTAs (M <= 128): 128 x 256 tiles, 4 stages.
+// Block-scaled kernels run one CTA per MMA: in CTA pairs every scale-writer
+// arrival on the leader's barrier is a cluster-scope release, which costs more
+// than the stage it guards.
+// NVFP4: 128 x 256 tiles, 4 stages, one TMEM accumulator (the scale slots use
+// the rest), epilogue staged in 32 x 32 chunks, single-buffered.
 using CfgNvfp4 = Config<KIND_NVFP4, 256, 4, 1, 32, 1, 1>;
-// MXFP8, CTA pairs (M > 128): 256 x 128 tiles, 7 stages, double-buffered accumulator.
-using CfgMxfp8Pair = Config<KIND_MXFP8, 128, 7, 2, 32, 1, 2>;
-// MXFP8, single CTAs (M <= 128, the skinny HBM-bound shape): 128 x 128 tiles, 6 stages.
+// MXFP8: 128 x 128 tiles, 6 stages, double-buffered accumulator.
 using CfgMxfp8 = Config<KIND_MXFP8, 128, 6, 2, 32, 1, 1>;
 
 static __device__ unsigned int g_err_bs;
@@ -39,7 +38,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
     constexpr bool fp4 = Cfg::KIND == KIND_NVFP4;
     const int64_t row_bytes = fp4 ? K / 2 : K;    // data bytes per row
     const int64_t sf_cols = K / (fp4 ? 16 : 32);  // scale bytes per row
-    CUtensorMap ta, tb, tsa, tsb, td;
+    CUtensorMap ta, tb, tsa, tsb, td, tc;
     // Data boxes: 128 bytes of K (256 E2M1 / 128 E4M3 elements) x rows, 128B swizzle;
     // A boxes are this CTA's 128 rows, B boxes its BN/PAIR rows.  Scale boxes: 16 bytes
     // (16 scale blocks) x rows, no swizzle: 128 SFA rows, all BN SFB rows of the tile.
@@ -50,6 +49,11 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
         !encode_tma_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, sf_cols, N, sf_cols, 16, Cfg::BN, 0) ||
         !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
                        Cfg::EPI_ROW_BYTES))
+        return GEMM_ERR_CUDA;
+    // C (if any): the same boxes as D, TMA-loaded into the epilogue staging buffers.
+    if (C == nullptr)
+        tc = td;
+    else if (!encode_tma_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, N * 2, Cfg::EPI_COLS, 32, Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (err == nullptr) return GEMM_ERR_CUDA;
@@ -63,7 +67,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
     p.C = C;
     p.D = D;
     p.err = err;
-    if (launch_config<Cfg>(ta, tb, tsa, tsb, td, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_config<Cfg>(ta, tb, tsa, tsb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -72,12 +76,8 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
 gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA,
                                        const void* B, const void* SFB, const void* C, void* D, int fmt,
                                        cudaStream_t stream, int sms, int dev) {
-    const bool pair = M > 128;
-    if (fmt == GEMM_FMT_NVFP4)
-        return pair ? run<CfgNvfp4Pair>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
-                    : run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
-    return pair ? run<CfgMxfp8Pair>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
-                : run<CfgMxfp8>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
+    if (fmt == GEMM_FMT_NVFP4) return run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
+    return run<CfgMxfp8>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
 }
 
 unsigned int read_clear_error_block_scaled() {

@@ -34,13 +34,18 @@ unsigned int* err_word(int dev) {
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
                   cudaStream_t stream, int sms, int dev) {
-    CUtensorMap ta, tb, td;
+    CUtensorMap ta, tb, td, tc;
     // A: fp16 [M][K], 128-row boxes; B: fp16 [N][K], BN/PAIR-row boxes; 64 elements
     // (128 bytes) of K per box.  D: fp16 [M][N], stored in 32-row x EPI_COLS boxes.
     if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, 64, Cfg::BM, 128) ||
         !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, 64, Cfg::BN_CTA, 128) ||
         !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
                        Cfg::EPI_ROW_BYTES))
+        return GEMM_ERR_CUDA;
+    // C (if any): the same boxes as D, TMA-loaded into the epilogue staging buffers.
+    if (C == nullptr)
+        tc = td;
+    else if (!encode_tma_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, Cfg::EPI_COLS, 32, Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (err == nullptr) return GEMM_ERR_CUDA;
@@ -54,7 +59,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
     p.C = C;
     p.D = D;
     p.err = err;
-    if (launch_config<Cfg>(ta, tb, ta, tb, td, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_config<Cfg>(ta, tb, ta, tb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

@@ -105,7 +105,8 @@ struct Config {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;  // 1024-byte aligned
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUFS * EPI_BUF_BYTES;
-    // barriers: full[S], empty[S], sf_full[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain
+    // barriers: full[S], empty[S], sf_full[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain,
+    // c_load[4][EPI_BUFS]
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = STAGES;
     static constexpr int BAR_SFFULL = 2 * STAGES;
@@ -113,7 +114,8 @@ struct Config {
     static constexpr int BAR_TFULL = 4 * STAGES;
     static constexpr int BAR_TEMPTY = 4 * STAGES + ACC_BUFS;
     static constexpr int BAR_DRAIN = 4 * STAGES + 2 * ACC_BUFS;
-    static constexpr int NUM_BARS = BAR_DRAIN + 1;
+    static constexpr int BAR_CLOAD = BAR_DRAIN + 1;  // [epilogue warp][staging buffer]: C chunk landed
+    static constexpr int NUM_BARS = BAR_CLOAD + 4 * EPI_BUFS;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM base address, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 
@@ -232,29 +234,28 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 }
 
 // One thread's share of an epilogue chunk: output row `row`, columns n .. n+COLS-1
-// of the tile, accumulator words r[0..COLS-1].  Adds C (read directly, only for
-// in-bounds rows / 8-column groups), rounds once, and writes the packed outputs to
-// row `lane` of the warp's staging buffer in the swizzled order the D tensor map
-// uses (16-byte chunk j of row l at chunk j ^ f(l)).
-template <int KIND, int COLS>
-__device__ __forceinline__ void stage_chunk(const Params& p, int row, int n, const uint32_t* r, uint8_t* buf,
-                                            int lane) {
+// of the tile, accumulator words r[0..COLS-1].  With kCStaged the warp's staging
+// buffer already holds the matching C chunk (TMA-loaded with the D tensor map's
+// swizzle; zero outside C); the thread adds its row of it in fp32, rounds once and
+// writes the result back in place: 16-byte chunk j of row l lives at chunk
+// j ^ f(l), the XOR swizzle the D tensor map uses.
+template <int KIND, int COLS, bool kCStaged>
+__device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int lane) {
     constexpr int VECS = COLS / 8;  // 16-byte output vectors per row
-    const bool has_c = p.C != nullptr && row < p.M;
-    const uint16_t* crow = static_cast<const uint16_t*>(p.C) + static_cast<size_t>(row) * p.N + n;
     const int swz = (COLS == 64) ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
     for (int v = 0; v < VECS; ++v) {
+        uint4* slot = reinterpret_cast<uint4*>(buf + lane * (COLS * 2) + ((v ^ swz) * 16));
         float f[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
-        if (has_c && n + 8 * v < p.N) {
+        if constexpr (kCStaged) {
             float c[8];
-            unpack8<KIND>(*reinterpret_cast<const uint4*>(crow + 8 * v), c);
+            unpack8<KIND>(*slot, c);
 #pragma unroll
             for (int i = 0; i < 8; ++i) f[i] += c[i];
         }
-        *reinterpret_cast<uint4*>(buf + lane * (COLS * 2) + ((v ^ swz) * 16)) = pack8<KIND>(f);
+        *slot = pack8<KIND>(f);
     }
 }
 
@@ -309,7 +310,8 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                   const __grid_constant__ CUtensorMap tmD, const Params p) {
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmC,
+                   const Params p) {
     constexpr int KIND = Cfg::KIND;
     constexpr int PAIR = Cfg::PAIR;
     constexpr int BN = Cfg::BN;
@@ -346,6 +348,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(bar(Cfg::BAR_TEMPTY + b), 4 * PAIR);  // one arrival per epilogue warp
         }
         mbar_init(bar(Cfg::BAR_DRAIN), 1);
+        for (int i = 0; i < 4 * Cfg::EPI_BUFS; ++i) mbar_init(bar(Cfg::BAR_CLOAD + i), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -353,6 +356,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
+        if (p.C != nullptr) tma_prefetch_desc(&tmC);
         if constexpr (kBS) {
             tma_prefetch_desc(&tmSFA);
             tma_prefetch_desc(&tmSFB);
@@ -590,23 +594,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp >= 4 && warp < 8) {
         // -------------------------------------------------------------- epilogue
         constexpr int EC = Cfg::EPI_COLS;
+        constexpr int EB = Cfg::EPI_BUFS;
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        uint8_t* stg = smem + Cfg::OFF_EPI + q * (Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
-        const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + q * (Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+        uint8_t* stg = smem + Cfg::OFF_EPI + q * (EB * Cfg::EPI_BUF_BYTES);
+        const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + q * (EB * Cfg::EPI_BUF_BYTES);
+        const bool has_c = p.C != nullptr;
+        uint32_t cph = 0;      // bit b: phase of this warp's C-load barrier for buffer b
+        uint32_t cpending = 0;  // bit b: a C load into buffer b has not been waited for
         int eb = 0;
         int t_local = 0;
-        for (int tile = cluster; tile < num_tiles; tile += num_clusters, ++t_local) {
+        // C chunk at column nc of rows m_warp.. into staging buffer b (lane 0); the
+        // buffer must no longer be read by an earlier store.
+        auto load_c = [&](int b, int nc, int m_warp) {
+            const uint32_t cb = bar(Cfg::BAR_CLOAD + q * EB + b);
+            mbar_arrive_expect_tx(cb, Cfg::EPI_BUF_BYTES);
+            tma_load_2d(stg_u32 + b * Cfg::EPI_BUF_BYTES, &tmC, cb, nc, m_warp);
+            cpending |= 1u << b;
+        };
+        bool ok = true;
+        for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters, ++t_local) {
             const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
             const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
-            const bool ok =
-                __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
-            if (!ok) break;
-            tc_fence_after_sync();
             int mb, nb;
             tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
             // first output row of this warp
             const int m_warp = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM + q * 32;
             const int n0 = nb * BN;
+            const bool rows_in = m_warp < p.M;
+            // C does not depend on the accumulator: fetch the first chunk early
+            if (has_c && rows_in && lane == 0) {
+                bulk_wait_group_read<EB - 1>();
+                load_c(eb, n0, m_warp);
+            }
+            ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
+            if (!ok) break;
+            tc_fence_after_sync();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += EC) {
@@ -616,19 +638,38 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if constexpr (EC == 64)
                     tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
-                if (m_warp >= p.M) continue;  // no row of this warp lies inside D
-                // the staging buffer is free once the store issued from it has read it
-                if (lane == 0) bulk_wait_group_read<Cfg::EPI_BUFS - 1>();
-                __syncwarp();
-                stage_chunk<KIND, EC>(p, m_warp + lane, n0 + c, r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
+                if (!rows_in) continue;  // no row of this warp lies inside D
+                const bool more = c + EC < BN && n0 + c + EC < p.N;
+                if (has_c) {
+                    if (EB == 2 && more && lane == 0) {
+                        bulk_wait_group_read<0>();  // the other buffer's last store has read it
+                        load_c(eb ^ 1, n0 + c + EC, m_warp);
+                    }
+                    ok = __all_sync(0xffffffffu,
+                                    wait_bar(bar(Cfg::BAR_CLOAD + q * EB + eb), (cph >> eb) & 1u, abort_flag, p.err));
+                    cph ^= 1u << eb;
+                    cpending &= ~(1u << eb);
+                    if (!ok) break;
+                    stage_chunk<KIND, EC, true>(r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
+                } else {
+                    // the staging buffer is free once the store issued from it has read it
+                    if (lane == 0) bulk_wait_group_read<EB - 1>();
+                    __syncwarp();
+                    stage_chunk<KIND, EC, false>(r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     tma_store_2d(&tmD, stg_u32 + eb * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
                     bulk_commit_group();
+                    if (has_c && EB == 1 && more) {
+                        bulk_wait_group_read<0>();
+                        load_c(eb, n0 + c + EC, m_warp);
+                    }
                 }
-                if constexpr (Cfg::EPI_BUFS == 2) eb ^= 1;
+                if constexpr (EB == 2) eb ^= 1;
             }
+            if (!ok) break;
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -638,7 +679,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
             }
         }
-        if (lane == 0) bulk_wait_group_all();
+        if (lane == 0) {
+            // Abandoning: let C loads still in flight land before the CTA exits.
+            for (int b = 0; b < EB; ++b)
+                if (cpending & (1u << b)) wait_bar_drain(bar(Cfg::BAR_CLOAD + q * EB + b), (cph >> b) & 1u);
+            bulk_wait_group_all();
+        }
         __syncwarp();
     }
 

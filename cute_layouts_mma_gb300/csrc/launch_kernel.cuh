@@ -19,8 +19,8 @@ std::atomic<int> LaunchState<Cfg>::max_units[kMaxDevices];
 
 template <class Cfg>
 cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                          const CUtensorMap& tsb, const CUtensorMap& td, const Params& p, int sms, int dev,
-                          cudaStream_t stream) {
+                          const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& tc, const Params& p,
+                          int sms, int dev, cudaStream_t stream) {
     auto kernel = tn_gemm_kernel<Cfg>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -53,7 +53,7 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     const int tiles = p.num_m_blocks * p.num_n_blocks;
     const int used = tiles < units ? tiles : units;
     cfg.gridDim = dim3(used * Cfg::PAIR, 1, 1);
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, p);
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, tc, p);
 }
 
 }  // namespace tn
