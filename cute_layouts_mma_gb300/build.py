@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtn_gemm.so")
+# Test-only variant: compiled with TN_TIMEOUT_INJECT, one pipeline arrival is
+# withheld so that a bounded wait runs out (exercises the abandon path).
+VARIANTS = {"timeout_inject": ["-DTN_TIMEOUT_INJECT"]}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
@@ -40,22 +43,33 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def lib_path(variant: str = "") -> str:
+    if not variant:
+        return LIB
+    return os.path.join(BUILD, variant, f"libtn_gemm_{variant}.so")
+
+
+def up_to_date(variant: str = "") -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
+    """Build the library (variant "" is the product; others are test builds)."""
+    lib = lib_path(variant)
+    if not force and up_to_date(variant):
+        return lib
+    outdir = os.path.dirname(lib)
+    os.makedirs(outdir, exist_ok=True)
     nvcc = _nvcc()
+    extra = VARIANTS[variant] if variant else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(outdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -66,13 +80,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for obj, log in results:
             sys.stderr.write(f"--- {os.path.basename(obj)}\n{log}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -403,6 +403,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ok = false;
                     break;
                 }
+#ifdef TN_TIMEOUT_INJECT
+                // Test build only: CTA 0's A issuer withholds its first stage, so the
+                // MMA thread's bounded wait on that stage runs out.
+                if (role == 0 && blockIdx.x == 0 && tile == cluster && kb == 0) {
+                    ++loads[s];
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    continue;
+                }
+#endif
                 if (role <= 1) {
                     const int kx = kb * Cfg::kKCoordPerStage;
                     const uint32_t dst = role == 0 ? sbase + Cfg::OFF_A + s * Cfg::A_BYTES
@@ -437,19 +449,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
         }
-        if (ok) {
-            if (role == 0) {
-                // Wait until the MMAs have released every stage, so that no
-                // tcgen05.commit arrival is still in flight when the CTA exits.
-                for (int i = 0; i < STAGES; ++i) {
-                    if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) break;
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+        if (ok && role == 0) {
+            // Wait until the MMAs have released every stage, so that no
+            // tcgen05.commit arrival is still in flight when the CTA exits.
+            for (int i = 0; i < STAGES && ok; ++i) {
+                ok = wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-        } else {
+        }
+        if (!ok) {
             // Abandoning: let every issued TMA copy land before the CTA exits.
             for (int i = 0; i < STAGES; ++i) {
                 if (loads[i] == 0) continue;

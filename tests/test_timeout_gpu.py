@@ -1,0 +1,85 @@
+"""Failure detection on the GPU without a fault: a bounded pipeline wait runs out.
+
+The test build of the library (compiled with TN_TIMEOUT_INJECT) withholds one
+producer arrival in CTA 0, so that CTA's MMA thread waits on a stage that can
+never fill.  The kernel must give up after its time limit, record the timeout,
+drain its in-flight copies, free TMEM and return: the host reads
+GEMM_ERR_TIMEOUT, the other CTA's tile is still computed exactly, and the CUDA
+context stays usable.
+
+The test build runs in a child process: two copies of the library (each with
+its own static CUDA runtime) cannot be used in one process.
+"""
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import textwrap
+
+import numpy as np
+import pytest
+import torch
+
+import cute_layouts_mma_gb300 as tg
+from cute_layouts_mma_gb300 import build as tg_build
+from cute_layouts_mma_gb300 import inputs
+
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = textwrap.dedent(r"""
+    import ctypes, json, sys, time
+    import numpy as np, torch
+    sys.path.insert(0, sys.argv[1])
+    from cute_layouts_mma_gb300 import build as b, inputs
+    lib = ctypes.CDLL(b.build(variant="timeout_inject"))
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.gemm_f16.argtypes = [i64, i64, i64, vp, vp, vp, vp, ci, vp]
+    lib.gemm_f16.restype = ci
+    lib.gemm_last_device_error.restype = ci
+    prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    dev = torch.device("cuda", 0)
+    A, B = prob["A"].to(dev), prob["B"].to(dev)
+    D = torch.zeros(128, 512, dtype=torch.float16, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    rc = lib.gemm_f16(128, 512, 256, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 0,
+                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    status = lib.gemm_last_device_error()
+    elapsed = time.time() - t0
+    again = lib.gemm_last_device_error()
+    # the context still works after the abandoned launch
+    x = torch.arange(1024, device=dev, dtype=torch.float32)
+    usable = float((x * 2).sum().item()) == float(1023 * 1024)
+    np.save(sys.argv[2], D.cpu().view(torch.int16).numpy())
+    print(json.dumps({"rc": rc, "status": status, "again": again, "elapsed": elapsed, "usable": usable}))
+""")
+
+
+def test_bounded_wait_runs_out_and_is_reported():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    with tempfile.TemporaryDirectory() as tmp:
+        script = os.path.join(tmp, "child.py")
+        out_npy = os.path.join(tmp, "d.npy")
+        with open(script, "w") as f:
+            f.write(CHILD)
+        r = subprocess.run([sys.executable, script, ROOT, out_npy], capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+        d_bits = np.load(out_npy).view(np.uint16)
+    assert res["rc"] == tg.GEMM_OK              # the launch itself was valid
+    assert res["status"] == tg.GEMM_ERR_TIMEOUT  # ... and the kernel gave up and said so
+    assert 1.0 <= res["elapsed"] < 60.0          # the per-wait limit is 2 s
+    assert res["again"] == tg.GEMM_OK            # the record is cleared once read
+    assert res["usable"]
+    # CTA 1's tile (columns 256..511) was not affected: exact against the oracle
+    prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    d16, _ = P.oracle_result(prob)
+    assert np.array_equal(d_bits[:, 256:], d16[:, 256:])
+    # and this process's product library is unaffected
+    P.check(prob, P.run_gpu(prob), mode="exact")
