@@ -6,13 +6,15 @@
 
 namespace tn {
 
-// Block-scaled kernels run one CTA per MMA: in CTA pairs every scale-writer
-// arrival on the leader's barrier is a cluster-scope release, which costs more
-// than the stage it guards.
-// NVFP4: 128 x 256 tiles, 4 stages, one TMEM accumulator (the scale slots use
-// the rest), epilogue staged in 32 x 32 chunks, single-buffered.
+// NVFP4, CTA pairs (M > 128): 256 x 256 tiles, 4 stages, one TMEM accumulator
+// (the scale slots use the rest); the epilogue stages a warp's whole 32 x 256
+// slice, so the accumulator is released before any store is issued.
+using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 4, 2>;
+// NVFP4, single CTAs (M <= 128): 128 x 256 tiles, 4 stages, epilogue staged in
+// 32 x 32 chunks, single-buffered.
 using CfgNvfp4 = Config<KIND_NVFP4, 256, 4, 1, 32, 1, 1>;
-// MXFP8: 128 x 128 tiles, 6 stages, double-buffered accumulator.
+// MXFP8: 128 x 128 tiles, 6 stages, double-buffered accumulator (one CTA per
+// MMA: the skinny, HBM-bound shape is M = 128).
 using CfgMxfp8 = Config<KIND_MXFP8, 128, 6, 2, 32, 1, 1>;
 
 static __device__ unsigned int g_err_bs;
@@ -76,7 +78,9 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
 gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA,
                                        const void* B, const void* SFB, const void* C, void* D, int fmt,
                                        cudaStream_t stream, int sms, int dev) {
-    if (fmt == GEMM_FMT_NVFP4) return run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
+    if (fmt == GEMM_FMT_NVFP4)
+        return M > 128 ? run<CfgNvfp4Pair>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
+                       : run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
     return run<CfgMxfp8>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
 }
 

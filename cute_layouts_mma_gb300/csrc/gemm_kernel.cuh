@@ -82,6 +82,9 @@ struct Config {
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
     static_assert(EPI_COLS == 32 || EPI_COLS == 64, "staging rows of 64 or 128 bytes");
     static_assert(BN % EPI_COLS == 0, "whole staging chunks per tile");
+    // Staging covers a warp's whole 32 x BN slice: the accumulator is drained to
+    // shared memory and released before any store is issued.
+    static constexpr bool kWholeTileStaging = EPI_COLS * EPI_BUFS == BN;
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
@@ -590,8 +593,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
+                        // The scales are TMEM data whose writes tcgen05.wait::st has
+                        // completed: the leader needs no release of generic memory.
                         if constexpr (kPair)
-                            mbar_arrive_cluster(leader_bar(Cfg::BAR_SF + s));
+                            mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_SF + s));
                         else
                             mbar_arrive(bar(Cfg::BAR_SF + s));
                     }
@@ -632,8 +637,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int m_warp = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM + q * 32;
             const int n0 = nb * BN;
             const bool rows_in = m_warp < p.M;
-            // C does not depend on the accumulator: fetch the first chunk early
-            if (has_c && rows_in && lane == 0) {
+            // C does not depend on the accumulator: fetch it early
+            if constexpr (Cfg::kWholeTileStaging) {
+                if (rows_in && lane == 0) {
+                    bulk_wait_group_read<0>();  // the previous tile's stores have read the buffers
+                    if (has_c)
+                        for (int c = 0, b = 0; c < BN && n0 + c < p.N; c += EC, ++b) load_c(b, n0 + c, m_warp);
+                }
+                __syncwarp();
+            } else if (has_c && rows_in && lane == 0) {
                 bulk_wait_group_read<EB - 1>();
                 load_c(eb, n0, m_warp);
             }
@@ -641,6 +653,51 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+            if constexpr (Cfg::kWholeTileStaging) {
+                // Drain every chunk into its own staging buffer, release the
+                // accumulator, then store: the MMAs of the next tile wait only for
+                // the TMEM reads.
+#pragma unroll 1
+                for (int c = 0, b = 0; c < BN; c += EC, ++b) {
+                    if (n0 + c >= p.N) break;  // warp-uniform
+                    uint32_t r[EC];
+                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    if constexpr (EC == 64)
+                        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32),
+                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_ld_wait();
+                    if (!rows_in) continue;
+                    if (has_c) {
+                        ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_CLOAD + q * EB + b), (cph >> b) & 1u,
+                                                              abort_flag, p.err));
+                        cph ^= 1u << b;
+                        cpending &= ~(1u << b);
+                        if (!ok) break;
+                        stage_chunk<KIND, EC, true>(r, stg + b * Cfg::EPI_BUF_BYTES, lane);
+                    } else {
+                        stage_chunk<KIND, EC, false>(r, stg + b * Cfg::EPI_BUF_BYTES, lane);
+                    }
+                }
+                if (!ok) break;
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                    else
+                        mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+                }
+                if (rows_in) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        for (int c = 0, b = 0; c < BN && n0 + c < p.N; c += EC, ++b)
+                            tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
+                        bulk_commit_group();
+                    }
+                }
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < BN; c += EC) {
                 if (n0 + c >= p.N) break;  // warp-uniform
