@@ -7,9 +7,9 @@
 namespace tn {
 
 // NVFP4, CTA pairs (M > 128): 256 x 256 tiles, 4 stages, one TMEM accumulator
-// (the scale slots use the rest); the epilogue stages a warp's whole 32 x 256
+// (the scale slots use the rest); 8 epilogue warps each stage a whole 32 x 128
 // slice, so the accumulator is released before any store is issued.
-using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 4, 2>;
+using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 2, 2, 8>;
 // NVFP4, single CTAs (M <= 128): 128 x 256 tiles, 4 stages, epilogue staged in
 // 32 x 32 chunks, single-buffered.
 using CfgNvfp4 = Config<KIND_NVFP4, 256, 4, 1, 32, 1, 1>;

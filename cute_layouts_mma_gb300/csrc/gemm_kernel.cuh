@@ -64,7 +64,8 @@ struct Params {
     unsigned int* err;
 };
 
-template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_>
+template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
+          int EPI_WARPS_ = 4>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
@@ -80,16 +81,22 @@ struct Config {
     static constexpr int EPI_BUFS = EPI_BUFS_;
     static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
+    // 4 epilogue warps (warps 4-7), or 8 (also warps 13-16): two per TMEM lane
+    // quarter, each draining half of the tile's columns.
+    static constexpr int EPI_WARPS = EPI_WARPS_;
+    static constexpr int EPI_SPLIT = EPI_WARPS / 4;      // column ranges per lane quarter
+    static constexpr int BN_EPI = BN / EPI_SPLIT;         // columns drained by one epilogue warp
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
     static_assert(EPI_COLS == 32 || EPI_COLS == 64, "staging rows of 64 or 128 bytes");
-    static_assert(BN % EPI_COLS == 0, "whole staging chunks per tile");
-    // Staging covers a warp's whole 32 x BN slice: the accumulator is drained to
-    // shared memory and released before any store is issued.
-    static constexpr bool kWholeTileStaging = EPI_COLS * EPI_BUFS == BN;
+    static_assert((BN / EPI_SPLIT) % EPI_COLS == 0, "whole staging chunks per epilogue warp");
+    // Staging covers a warp's whole 32-row slice of the tile: the accumulator is
+    // drained to shared memory and released before any store is issued.
+    static constexpr bool kWholeTileStaging = EPI_COLS * EPI_BUFS == BN / EPI_SPLIT;
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
-    // writers, 12 SFB issuer
-    static constexpr int THREADS = kBlockScaled ? 416 : 256;
+    // writers, 12 SFB issuer, 13-16 second epilogue set
+    static constexpr int THREADS = EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256);
     static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
     static constexpr int kKCoordPerStage = (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) ? 64 : 128;
@@ -107,9 +114,9 @@ struct Config {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;  // 1024-byte aligned
-    static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUFS * EPI_BUF_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
     // barriers: full[S], empty[S], sf_full[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain,
-    // c_load[4][EPI_BUFS]
+    // c_load[EPI_WARPS][EPI_BUFS]
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = STAGES;
     static constexpr int BAR_SFFULL = 2 * STAGES;
@@ -118,7 +125,7 @@ struct Config {
     static constexpr int BAR_TEMPTY = 4 * STAGES + ACC_BUFS;
     static constexpr int BAR_DRAIN = 4 * STAGES + 2 * ACC_BUFS;
     static constexpr int BAR_CLOAD = BAR_DRAIN + 1;  // [epilogue warp][staging buffer]: C chunk landed
-    static constexpr int NUM_BARS = BAR_CLOAD + 4 * EPI_BUFS;
+    static constexpr int NUM_BARS = BAR_CLOAD + EPI_WARPS * EPI_BUFS;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM base address, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 
@@ -348,10 +355,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(bar(Cfg::BAR_TFULL + b), 1);
-            mbar_init(bar(Cfg::BAR_TEMPTY + b), 4 * PAIR);  // one arrival per epilogue warp
+            mbar_init(bar(Cfg::BAR_TEMPTY + b), Cfg::EPI_WARPS * PAIR);  // one arrival per epilogue warp
         }
         mbar_init(bar(Cfg::BAR_DRAIN), 1);
-        for (int i = 0; i < 4 * Cfg::EPI_BUFS; ++i) mbar_init(bar(Cfg::BAR_CLOAD + i), 1);
+        for (int i = 0; i < Cfg::EPI_WARPS * Cfg::EPI_BUFS; ++i) mbar_init(bar(Cfg::BAR_CLOAD + i), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -607,13 +614,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if ((warp >= 4 && warp < 8) || (Cfg::EPI_WARPS == 8 && warp >= 13 && warp < 17)) {
         // -------------------------------------------------------------- epilogue
         constexpr int EC = Cfg::EPI_COLS;
         constexpr int EB = Cfg::EPI_BUFS;
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        uint8_t* stg = smem + Cfg::OFF_EPI + q * (EB * Cfg::EPI_BUF_BYTES);
-        const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + q * (EB * Cfg::EPI_BUF_BYTES);
+        const int q = warp & 3;                       // TMEM lane quarter this warp may access
+        const int e = warp < 8 ? warp - 4 : warp - 9;  // epilogue warp index
+        const int c_begin = (e >> 2) * Cfg::BN_EPI;    // this warp's columns of the tile
+        const int c_end = c_begin + Cfg::BN_EPI;
+        uint8_t* stg = smem + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
+        const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
         const bool has_c = p.C != nullptr;
         uint32_t cph = 0;      // bit b: phase of this warp's C-load barrier for buffer b
         uint32_t cpending = 0;  // bit b: a C load into buffer b has not been waited for
@@ -622,7 +632,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // C chunk at column nc of rows m_warp.. into staging buffer b (lane 0); the
         // buffer must no longer be read by an earlier store.
         auto load_c = [&](int b, int nc, int m_warp) {
-            const uint32_t cb = bar(Cfg::BAR_CLOAD + q * EB + b);
+            const uint32_t cb = bar(Cfg::BAR_CLOAD + e * EB + b);
             mbar_arrive_expect_tx(cb, Cfg::EPI_BUF_BYTES);
             tma_load_2d(stg_u32 + b * Cfg::EPI_BUF_BYTES, &tmC, cb, nc, m_warp);
             cpending |= 1u << b;
@@ -642,12 +652,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (rows_in && lane == 0) {
                     bulk_wait_group_read<0>();  // the previous tile's stores have read the buffers
                     if (has_c)
-                        for (int c = 0, b = 0; c < BN && n0 + c < p.N; c += EC, ++b) load_c(b, n0 + c, m_warp);
+                        for (int c = c_begin, b = 0; c < c_end && n0 + c < p.N; c += EC, ++b) load_c(b, n0 + c, m_warp);
                 }
                 __syncwarp();
-            } else if (has_c && rows_in && lane == 0) {
+            } else if (has_c && rows_in && lane == 0 && n0 + c_begin < p.N) {
                 bulk_wait_group_read<EB - 1>();
-                load_c(eb, n0, m_warp);
+                load_c(eb, n0 + c_begin, m_warp);
             }
             ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
             if (!ok) break;
@@ -658,7 +668,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // accumulator, then store: the MMAs of the next tile wait only for
                 // the TMEM reads.
 #pragma unroll 1
-                for (int c = 0, b = 0; c < BN; c += EC, ++b) {
+                for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
                     if (n0 + c >= p.N) break;  // warp-uniform
                     uint32_t r[EC];
                     tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -668,7 +678,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tmem_ld_wait();
                     if (!rows_in) continue;
                     if (has_c) {
-                        ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_CLOAD + q * EB + b), (cph >> b) & 1u,
+                        ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_CLOAD + e * EB + b), (cph >> b) & 1u,
                                                               abort_flag, p.err));
                         cph ^= 1u << b;
                         cpending &= ~(1u << b);
@@ -691,7 +701,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        for (int c = 0, b = 0; c < BN && n0 + c < p.N; c += EC, ++b)
+                        for (int c = c_begin, b = 0; c < c_end && n0 + c < p.N; c += EC, ++b)
                             tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
                         bulk_commit_group();
                     }
@@ -699,7 +709,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 continue;
             }
 #pragma unroll 1
-            for (int c = 0; c < BN; c += EC) {
+            for (int c = c_begin; c < c_end; c += EC) {
                 if (n0 + c >= p.N) break;  // warp-uniform
                 uint32_t r[EC];
                 tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -707,14 +717,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
                 if (!rows_in) continue;  // no row of this warp lies inside D
-                const bool more = c + EC < BN && n0 + c + EC < p.N;
+                const bool more = c + EC < c_end && n0 + c + EC < p.N;
                 if (has_c) {
                     if (EB == 2 && more && lane == 0) {
                         bulk_wait_group_read<0>();  // the other buffer's last store has read it
                         load_c(eb ^ 1, n0 + c + EC, m_warp);
                     }
                     ok = __all_sync(0xffffffffu,
-                                    wait_bar(bar(Cfg::BAR_CLOAD + q * EB + eb), (cph >> eb) & 1u, abort_flag, p.err));
+                                    wait_bar(bar(Cfg::BAR_CLOAD + e * EB + eb), (cph >> eb) & 1u, abort_flag, p.err));
                     cph ^= 1u << eb;
                     cpending &= ~(1u << eb);
                     if (!ok) break;
@@ -750,7 +760,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (lane == 0) {
             // Abandoning: let C loads still in flight land before the CTA exits.
             for (int b = 0; b < EB; ++b)
-                if (cpending & (1u << b)) wait_bar_drain(bar(Cfg::BAR_CLOAD + q * EB + b), (cph >> b) & 1u);
+                if (cpending & (1u << b)) wait_bar_drain(bar(Cfg::BAR_CLOAD + e * EB + b), (cph >> b) & 1u);
             bulk_wait_group_all();
         }
         __syncwarp();
