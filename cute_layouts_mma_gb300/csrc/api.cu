@@ -97,6 +97,27 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
     return true;
 }
 
+namespace {
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+}  // namespace
+
+cudaMemPool_t scratch_pool(int dev) {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (g_pools[dev] == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        uint64_t keep = UINT64_MAX;  // keep the memory in the pool between calls
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pools[dev] = pool;
+    }
+    return g_pools[dev];
+}
+
 }  // namespace tn
 
 extern "C" {

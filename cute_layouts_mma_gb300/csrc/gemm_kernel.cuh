@@ -62,7 +62,60 @@ struct Params {
     const void* C;  // [M][N] fp16 (FP16 kinds) or bf16 (block-scaled), or null
     void* D;        // [M][N], same type as C
     unsigned int* err;
+    // Stream-K schedule: the last sk_tiles tiles (in tile order) are split across
+    // all units, each taking an equal contiguous share of their (tile, k-block)
+    // sequence before its whole tiles.  A tile cut between units is finished by
+    // the unit holding its k-block 0 (that piece ends the unit's share); the later
+    // pieces, which begin the next units' shares, leave fp32 partial sums in `ws`
+    // and raise their flag.  The remaining tiles are dealt whole, round robin.
+    int sk_tiles;          // 0: every tile whole
+    long long sk_total;    // sk_tiles * num_k_blocks
+    float* ws;             // partials: [unit][rank][epilogue warp][chunk][col/4][lane][4]
+    unsigned int* flags;   // [unit][rank][epilogue warp]: 1 once that partial is written
 };
+
+enum SegKind : int { SEG_FULL = 0, SEG_PARTIAL = 1, SEG_OWNER = 2 };
+
+// The work of one unit as a sequence of segments: tile, k blocks [k0, k1), kind.
+struct SegIter {
+    long long pos, end;  // remaining stream-K share of the split tiles' (tile, k) sequence
+    int tile;            // next whole tile
+};
+
+__device__ __forceinline__ long long sk_share_begin(const Params& p, int unit, int units) {
+    return p.sk_total * unit / units;
+}
+
+__device__ __forceinline__ void seg_begin(const Params& p, int unit, int units, SegIter& it) {
+    it.pos = sk_share_begin(p, unit, units);
+    it.end = sk_share_begin(p, unit + 1, units);
+    it.tile = unit;
+}
+
+// SK = false compiles the whole-tile schedule alone.
+template <bool SK>
+__device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it, int& tile, int& k0, int& k1,
+                                         int& kind) {
+    const int nkb = p.num_k_blocks;
+    const int whole_tiles = p.num_m_blocks * p.num_n_blocks - (SK ? p.sk_tiles : 0);
+    if (SK && it.pos < it.end) {
+        const int t = static_cast<int>(it.pos / nkb);
+        tile = whole_tiles + t;
+        k0 = static_cast<int>(it.pos - static_cast<long long>(t) * nkb);
+        const long long rem = it.end - it.pos;
+        k1 = rem < static_cast<long long>(nkb - k0) ? k0 + static_cast<int>(rem) : nkb;
+        kind = k0 == 0 ? (k1 == nkb ? SEG_FULL : SEG_OWNER) : SEG_PARTIAL;
+        it.pos += k1 - k0;
+        return true;
+    }
+    if (it.tile >= whole_tiles) return false;
+    tile = it.tile;
+    k0 = 0;
+    k1 = nkb;
+    kind = SEG_FULL;
+    it.tile += units;
+    return true;
+}
 
 template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
           int EPI_WARPS_ = 4>
@@ -79,6 +132,9 @@ struct Config {
     // (64 or 128 bytes per row, 64B / 128B swizzle), EPI_BUFS buffers deep.
     static constexpr int EPI_COLS = EPI_COLS_;
     static constexpr int EPI_BUFS = EPI_BUFS_;
+    // Stream-K needs fp32 accumulation (partials are fp32 sums); the 8-epilogue-warp
+    // configuration has no registers to spare for it and stays data-parallel.
+    static constexpr bool kStreamK = KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4;
     static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
     // 4 epilogue warps (warps 4-7), or 8 (also warps 13-16): two per TMEM lane
@@ -316,6 +372,34 @@ __device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t
     }
 }
 
+// Stream-K partial slot of one epilogue warp: 32 rows x BN_EPI fp32 sums laid out
+// [chunk][col/4][lane][4], so that a warp's float4 accesses are 512 contiguous bytes.
+template <class Cfg>
+__device__ __forceinline__ float4* partial_slot(const Params& p, int unit, uint32_t rank, int e) {
+    const size_t idx = (static_cast<size_t>(unit) * Cfg::PAIR + rank) * Cfg::EPI_WARPS + e;
+    return reinterpret_cast<float4*>(p.ws) + idx * (32 * Cfg::BN_EPI / 4);
+}
+
+template <class Cfg>
+__device__ __forceinline__ unsigned int* partial_flag(const Params& p, int unit, uint32_t rank, int e) {
+    return p.flags + (static_cast<size_t>(unit) * Cfg::PAIR + rank) * Cfg::EPI_WARPS + e;
+}
+
+// Wait (lane 0 of the warp, bounded) until a peer unit has published its partial.
+__device__ __forceinline__ bool wait_flag(const unsigned int* f, volatile int* abort_flag, unsigned int* err) {
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(f) != 1u) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, 1u);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -389,9 +473,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_slot;
 
-    const int num_tiles = p.num_m_blocks * p.num_n_blocks;
-    const int nkb = p.num_k_blocks;
-
     // ------------------------------------------------------------------ TMA issuers
     // role 0: A, 1: B, 2: SFA, 3: SFB.  Each waits for its stage slot to be released
     // by the MMAs that last read it, arms its barrier with its bytes and issues one box.
@@ -402,13 +483,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < STAGES; ++i) loads[i] = 0;
         bool ok = true;
-        for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
+        SegIter it;
+        seg_begin(p, cluster, num_clusters, it);
+        int tile, k0, k1, kind;
+        bool first_seg = true;
+        while (ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind)) {
             int mb, nb;
             tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
             const int m0 = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM;  // this CTA's A rows
             const int nb0 = nb * BN;                                              // tile's first column
             const int n0 = nb0 + static_cast<int>(rank) * Cfg::BN_CTA;           // this CTA's B rows
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = k0; kb < k1; ++kb) {
                 if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -416,7 +501,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #ifdef TN_TIMEOUT_INJECT
                 // Test build only: CTA 0's A issuer withholds its first stage, so the
                 // MMA thread's bounded wait on that stage runs out.
-                if (role == 0 && blockIdx.x == 0 && tile == cluster && kb == 0) {
+                if (role == 0 && blockIdx.x == 0 && first_seg && kb == k0) {
                     ++loads[s];
                     if (++s == STAGES) {
                         s = 0;
@@ -458,7 +543,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ph ^= 1u;
                 }
             }
+            first_seg = false;
         }
+        (void)kind;
         if (ok && role == 0) {
             // Wait until the MMAs have released every stage, so that no
             // tcgen05.commit arrival is still in flight when the CTA exits.
@@ -492,7 +579,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // One thread issues every MMA; each tcgen05 instruction costs it tens of
             // cycles, so the loop keeps its own bookkeeping incremental (no divisions)
             // and the shared-memory descriptors precomputed.
-            const int my_tiles = cluster < num_tiles ? (num_tiles - 1 - cluster) / num_clusters + 1 : 0;
             constexpr uint32_t kM = 128 * PAIR;
             // descriptor of stage 0; stage s adds s * (bytes / 16) to the start address
             const uint64_t adesc0 = smem_desc_sw128(sbase + Cfg::OFF_A);
@@ -500,7 +586,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             bool ok = true;
             int s = 0;
             uint32_t ph = 0;
-            for (int t_local = 0; t_local < my_tiles && ok; ++t_local) {
+            SegIter it;
+            seg_begin(p, cluster, num_clusters, it);
+            int tile, k0, k1, kind;
+            for (int t_local = 0; ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind); ++t_local) {
                 const int buf = (ACC_BUFS == 1) ? 0 : (t_local & 1);
                 const uint32_t use = static_cast<uint32_t>(ACC_BUFS == 1 ? t_local : (t_local >> 1));
                 if (!wait_bar<kPair>(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
@@ -508,7 +597,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
+                    const bool acc_kb = kb != k0;  // the first k block of a segment starts from 0
                     if (!wait_bar<kPair>(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -527,9 +617,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             if constexpr (kPair)
-                                mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                                mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
                             else
-                                mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                                mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
                         }
                     } else {
                         const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
@@ -539,9 +629,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             for (int j = 0; j < 4; ++j) {
                                 const uint32_t t = sf_tmem + j * Cfg::SF_COLS_PER_COPYSET;
                                 if constexpr (kPair)
-                                    mma_mxf4nvf4_4x_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, (kb | j) != 0);
+                                    mma_mxf4nvf4_4x_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, acc_kb || j != 0);
                                 else
-                                    mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, (kb | j) != 0);
+                                    mma_mxf4nvf4_4x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, t, t + 4, acc_kb || j != 0);
                             }
                         } else {
 #pragma unroll
@@ -550,10 +640,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                 const uint32_t idesc = idesc0 | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
                                 if constexpr (kPair)
                                     mma_mxf8f6f4_1x_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
-                                                         (kb | j) != 0);
+                                                         acc_kb || j != 0);
                                 else
                                     mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
-                                                    (kb | j) != 0);
+                                                    acc_kb || j != 0);
                             }
                         }
                     }
@@ -566,6 +656,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ph ^= 1u;
                     }
                 }
+                (void)tile;
+                (void)kind;
                 if (!ok) break;
                 if constexpr (kPair)
                     tc_commit_pair(bar(Cfg::BAR_TFULL + buf), 0x3);
@@ -589,8 +681,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
-                for (int kb = 0; kb < nkb; ++kb) {
+            SegIter it;
+            seg_begin(p, cluster, num_clusters, it);
+            int tile, k0, k1, kind;
+            while (ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind)) {
+                for (int kb = k0; kb < k1; ++kb) {
                     ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_SFFULL + s), ph, abort_flag, p.err));
                     if (!ok) break;
                     write_scales<KIND, Cfg::SFB_GROUPS>(
@@ -638,7 +733,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             cpending |= 1u << b;
         };
         bool ok = true;
-        for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters, ++t_local) {
+        constexpr bool kSK = Cfg::kStreamK;
+        SegIter it;
+        seg_begin(p, cluster, num_clusters, it);
+        int tile, k0, k1, kind;
+        for (; ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind); ++t_local) {
             const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
             const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
             int mb, nb;
@@ -647,6 +746,72 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int m_warp = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM + q * 32;
             const int n0 = nb * BN;
             const bool rows_in = m_warp < p.M;
+            (void)k0;
+            if (kSK && kind == SEG_PARTIAL) {
+                // A later piece of a tile another unit finishes: publish the fp32 sums.
+                ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t tacc =
+                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+                float4* slot = partial_slot<Cfg>(p, cluster, rank, e);
+#pragma unroll 1
+                for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
+                    uint32_t r[EC];
+                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    if constexpr (EC == 64)
+                        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32),
+                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < EC / 4; ++j)
+                        __stcg(slot + (b * (EC / 4) + j) * 32 + lane,
+                               make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+                }
+                __threadfence();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                    else
+                        mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+                    st_release_gpu(partial_flag<Cfg>(p, cluster, rank, e), 1u);
+                }
+                continue;
+            }
+            // Owner of a cut tile: the units after this one hold its later pieces.
+            int first_peer = 0, last_peer = -1;
+            if (kSK && kind == SEG_OWNER) {
+                first_peer = cluster + 1;
+                last_peer = first_peer;
+                const int split_index = tile - (p.num_m_blocks * p.num_n_blocks - p.sk_tiles);
+                const long long tile_end = static_cast<long long>(split_index + 1) * p.num_k_blocks;
+                while (last_peer + 1 < num_clusters && sk_share_begin(p, last_peer + 1, num_clusters) < tile_end)
+                    ++last_peer;
+                bool got = true;
+                if (lane == 0)
+                    for (int u = first_peer; u <= last_peer && got; ++u)
+                        got = wait_flag(partial_flag<Cfg>(p, u, rank, e), abort_flag, p.err);
+                ok = __all_sync(0xffffffffu, __shfl_sync(0xffffffffu, got, 0));
+                if (!ok) break;
+                __syncwarp();  // orders the lanes' partial reads after lane 0's acquire
+            }
+            // fp32 sums of the later pieces of this chunk, added to the accumulator
+            auto add_partials = [&](uint32_t* r, int b) {
+                for (int u = first_peer; u <= last_peer; ++u) {
+                    const float4* slot = partial_slot<Cfg>(p, u, rank, e);
+#pragma unroll
+                    for (int j = 0; j < EC / 4; ++j) {
+                        const float4 v = __ldcg(slot + (b * (EC / 4) + j) * 32 + lane);
+                        r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                        r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                        r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                        r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                    }
+                }
+            };
             // C does not depend on the accumulator: fetch it early
             if constexpr (Cfg::kWholeTileStaging) {
                 if (rows_in && lane == 0) {
@@ -677,6 +842,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                            *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                     tmem_ld_wait();
                     if (!rows_in) continue;
+                    if constexpr (kSK) add_partials(r, b);
                     if (has_c) {
                         ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_CLOAD + e * EB + b), (cph >> b) & 1u,
                                                               abort_flag, p.err));
@@ -706,55 +872,57 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         bulk_commit_group();
                     }
                 }
-                continue;
-            }
+            } else {
 #pragma unroll 1
-            for (int c = c_begin; c < c_end; c += EC) {
-                if (n0 + c >= p.N) break;  // warp-uniform
-                uint32_t r[EC];
-                tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                if constexpr (EC == 64)
-                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                tmem_ld_wait();
-                if (!rows_in) continue;  // no row of this warp lies inside D
-                const bool more = c + EC < c_end && n0 + c + EC < p.N;
-                if (has_c) {
-                    if (EB == 2 && more && lane == 0) {
-                        bulk_wait_group_read<0>();  // the other buffer's last store has read it
-                        load_c(eb ^ 1, n0 + c + EC, m_warp);
+                for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
+                    if (n0 + c >= p.N) break;  // warp-uniform
+                    uint32_t r[EC];
+                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    if constexpr (EC == 64)
+                        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32),
+                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_ld_wait();
+                    if (!rows_in) continue;  // no row of this warp lies inside D
+                    if constexpr (kSK) add_partials(r, b);
+                    const bool more = c + EC < c_end && n0 + c + EC < p.N;
+                    if (has_c) {
+                        if (EB == 2 && more && lane == 0) {
+                            bulk_wait_group_read<0>();  // the other buffer's last store has read it
+                            load_c(eb ^ 1, n0 + c + EC, m_warp);
+                        }
+                        ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_CLOAD + e * EB + eb), (cph >> eb) & 1u,
+                                                              abort_flag, p.err));
+                        cph ^= 1u << eb;
+                        cpending &= ~(1u << eb);
+                        if (!ok) break;
+                        stage_chunk<KIND, EC, true>(r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
+                    } else {
+                        // the staging buffer is free once the store issued from it has read it
+                        if (lane == 0) bulk_wait_group_read<EB - 1>();
+                        __syncwarp();
+                        stage_chunk<KIND, EC, false>(r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
                     }
-                    ok = __all_sync(0xffffffffu,
-                                    wait_bar(bar(Cfg::BAR_CLOAD + e * EB + eb), (cph >> eb) & 1u, abort_flag, p.err));
-                    cph ^= 1u << eb;
-                    cpending &= ~(1u << eb);
-                    if (!ok) break;
-                    stage_chunk<KIND, EC, true>(r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
-                } else {
-                    // the staging buffer is free once the store issued from it has read it
-                    if (lane == 0) bulk_wait_group_read<EB - 1>();
+                    fence_proxy_async_smem();
                     __syncwarp();
-                    stage_chunk<KIND, EC, false>(r, stg + eb * Cfg::EPI_BUF_BYTES, lane);
+                    if (lane == 0) {
+                        tma_store_2d(&tmD, stg_u32 + eb * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
+                        bulk_commit_group();
+                        if (has_c && EB == 1 && more) {
+                            bulk_wait_group_read<0>();
+                            load_c(eb, n0 + c + EC, m_warp);
+                        }
+                    }
+                    if constexpr (EB == 2) eb ^= 1;
                 }
-                fence_proxy_async_smem();
+                if (!ok) break;
+                tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmD, stg_u32 + eb * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
-                    bulk_commit_group();
-                    if (has_c && EB == 1 && more) {
-                        bulk_wait_group_read<0>();
-                        load_c(eb, n0 + c + EC, m_warp);
-                    }
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                    else
+                        mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
                 }
-                if constexpr (EB == 2) eb ^= 1;
-            }
-            if (!ok) break;
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (kPair)
-                    mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
-                else
-                    mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
             }
         }
         if (lane == 0) {

@@ -3,11 +3,37 @@
 #pragma once
 
 #include <atomic>
+#include <cstdint>
+#include <mutex>
 
 #include "gemm_kernel.cuh"
 #include "launch.h"
 
 namespace tn {
+
+// Stream-K is used when whole tiles would leave more than three quarters of the
+// units idle, each unit's share is at least kStreamKMinShare k-blocks, and the
+// accumulation is fp32.  Outside that range, measurement on GB300 favoured whole
+// tiles: once a quarter of the SMs stream operands, skinny problems are bound by
+// HBM rather than by SM count; dense FP16 runs at the power limit, where idle SMs
+// raise the clock of the busy ones; and short shares leave each split tile in many
+// pieces whose partials the finishing unit adds one after another.
+constexpr double kStreamKMinIdle = 0.75;
+constexpr long long kStreamKMinShare = 12;
+
+// Scratch of a stream-K launch: fp32 partial sums and per-warp flags.
+template <class Cfg>
+constexpr size_t sk_partial_bytes(int units) {
+    return static_cast<size_t>(units) * Cfg::PAIR * Cfg::BM * Cfg::BN * sizeof(float);
+}
+template <class Cfg>
+constexpr size_t sk_flag_bytes(int units) {
+    return (static_cast<size_t>(units) * Cfg::PAIR * Cfg::EPI_WARPS * sizeof(unsigned int) + 255) & ~size_t(255);
+}
+
+// Per-device stream-ordered pool the stream-K scratch is taken from (memory stays
+// with the pool between calls; each call's block is returned on its stream).
+cudaMemPool_t scratch_pool(int dev);
 
 // Per-device, per-configuration launch state, set up on first use.
 template <class Cfg>
@@ -17,9 +43,28 @@ struct LaunchState {
 template <class Cfg>
 std::atomic<int> LaunchState<Cfg>::max_units[kMaxDevices];
 
+// Schedule of one launch: units used and how many tiles (the last ones) are split.
+struct Schedule {
+    int units;
+    int sk_tiles;
+};
+
+template <class Cfg>
+Schedule choose_schedule(const Params& p, int max_units) {
+    const long long tiles = static_cast<long long>(p.num_m_blocks) * p.num_n_blocks;
+    Schedule sc{static_cast<int>(tiles < max_units ? tiles : max_units), 0};
+    if (!Cfg::kStreamK) return sc;
+    const long long rounds = (tiles + max_units - 1) / max_units;
+    const double idle = 1.0 - static_cast<double>(tiles) / static_cast<double>(rounds * max_units);
+    if (idle <= kStreamKMinIdle) return sc;
+    const long long split = tiles % max_units;  // the tiles of the last, partly idle round
+    if (split * p.num_k_blocks < kStreamKMinShare * max_units) return sc;
+    return Schedule{max_units, static_cast<int>(split)};
+}
+
 template <class Cfg>
 cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                          const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& tc, const Params& p,
+                          const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& tc, Params p,
                           int sms, int dev, cudaStream_t stream) {
     auto kernel = tn_gemm_kernel<Cfg>;
     cudaLaunchConfig_t cfg = {};
@@ -50,10 +95,25 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
         }
         LaunchState<Cfg>::max_units[dev].store(units, std::memory_order_release);
     }
-    const int tiles = p.num_m_blocks * p.num_n_blocks;
-    const int used = tiles < units ? tiles : units;
-    cfg.gridDim = dim3(used * Cfg::PAIR, 1, 1);
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, tc, p);
+    const Schedule sc = choose_schedule<Cfg>(p, units);
+    cfg.gridDim = dim3(sc.units * Cfg::PAIR, 1, 1);
+    p.sk_tiles = sc.sk_tiles;
+    p.sk_total = static_cast<long long>(sc.sk_tiles) * p.num_k_blocks;
+    p.ws = nullptr;
+    p.flags = nullptr;
+    if (sc.sk_tiles == 0) return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, tc, p);
+    // Stream-K scratch: taken from the device's stream-ordered pool for this call
+    // and returned on the same stream after the kernel.
+    const size_t pbytes = sk_partial_bytes<Cfg>(sc.units), fbytes = sk_flag_bytes<Cfg>(sc.units);
+    void* scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, pbytes + fbytes, scratch_pool(dev), stream);
+    if (e != cudaSuccess) return e;
+    p.ws = static_cast<float*>(scratch);
+    p.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(scratch) + pbytes);
+    e = cudaMemsetAsync(p.flags, 0, fbytes, stream);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, tc, p);
+    const cudaError_t f = cudaFreeAsync(scratch, stream);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace tn

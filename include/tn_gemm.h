@@ -15,7 +15,16 @@
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller; the
- *     library never frees, keeps or allocates device memory for a call.
+ *     library never frees or keeps caller memory.
+ *   - Scratch: when the output tiles do not fill whole rounds of the device's
+ *     SMs, fp32 accumulation uses a stream-K schedule (units split the k-blocks
+ *     of the tiles evenly; a tile cut between units is summed through fp32
+ *     partials in scratch memory).  That scratch (128 KB per SM at most, about
+ *     19.5 MB on 152 SMs) is taken with cudaMallocFromPoolAsync on `stream`
+ *     from a per-device memory pool the library creates on first need, and
+ *     returned to the pool with cudaFreeAsync on `stream` after the kernel; the
+ *     pool keeps its memory for later calls until the process exits.  A failed
+ *     allocation returns GEMM_ERR_CUDA and launches nothing.
  *   - Matrices are dense and row-major with no padding: A rows are K elements
  *     long (NVFP4: K/2 bytes), B rows likewise, C and D rows are N elements.
  *     Scale-factor matrices are row-major u8 [rows][K / K_blk].
@@ -34,7 +43,10 @@
  *
  * Numerics: products are formed by the tensor cores
  * and summed in fp32 (GEMM_ACC_F32) or fp16 (GEMM_ACC_F16); C is added in fp32
- * and the result rounded once, to nearest even, to the output type.
+ * and the result rounded once, to nearest even, to the output type.  Under the
+ * stream-K schedule the fp32 sum of a cut tile is formed piecewise (contiguous
+ * k-ranges, added in fp32), so the order of the fp32 additions depends on M, N,
+ * K and the SM count; results are deterministic for a given device and shape.
  */
 #ifndef TN_GEMM_H
 #define TN_GEMM_H

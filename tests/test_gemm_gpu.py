@@ -185,6 +185,62 @@ def test_mxfp8_128x16384_full_size_sampled_rows():
     assert torch.isfinite(D.float()).all()
 
 
+# ------------------------------------------------------------------ stream-K schedule
+# Skinny shapes with long K, whose whole tiles would leave most of the device
+# idle: the fp32 kinds split each tile's k-blocks between several units (with
+# 60..152 units these all take the stream-K schedule, each tile cut into two or
+# more pieces, so owners add one or several partials).  Integer-valued inputs
+# keep every fp32 partial sum exact, so the piecewise sum must match bit for bit.
+
+@pytest.mark.parametrize("M,N,K,with_c", [(128, 2560, 16384, True), (500, 760, 16384, True),
+                                          (64, 2056, 24576, False), (1, 4096, 16384, True)])
+def test_stream_k_fp16_integers_bit_exact(M, N, K, with_c):
+    prob = inputs.make_problem("f16", M, N, K, seed=M + N + K, dist="int2", with_c=with_c)
+    P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 24, seed=1), mode="exact")
+
+
+def test_stream_k_fp16_in_place():
+    prob = inputs.make_problem("f16", 300, 520, 16384, seed=21, dist="int2", with_c=True)
+    g = P.to_device(prob, P.device())
+    D = g["C"].clone()
+    tg.gemm_f16(g["A"], g["B"], D, D, tg.GEMM_ACC_F32)
+    torch.cuda.synchronize()
+    P.check(prob, D.cpu(), rows=P.sample_rows(300, 24, seed=6), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 1000, 16384), (129, 264, 65536)])
+def test_stream_k_fp16_random_tolerance(M, N, K):
+    prob = inputs.make_problem("f16", M, N, K, seed=M + K, dist="normal0.1", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 24, seed=2), mode="tol")
+
+
+def test_stream_k_repeatable_across_calls_and_streams():
+    # the scratch pool hands back blocks from earlier calls: results must not depend on them
+    prob = inputs.make_problem("f16", 500, 760, 16384, seed=22, dist="normal0.1", with_c=True)
+    first = P.run_gpu(prob, accum=0)
+    s = torch.cuda.Stream()
+    for stream in (None, s, None):
+        again = P.run_gpu(prob, accum=0, stream=stream)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K,with_c", [(128, 2048, 65536, True), (100, 3000, 65536, False)])
+def test_stream_k_nvfp4_integers_bit_exact(M, N, K, with_c):
+    prob = inputs.make_problem("nvfp4", M, N, K, seed=M + N, dist="int", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), rows=P.sample_rows(M, 12, seed=3), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K,with_c", [(100, 2048, 24576, True), (128, 1928, 24576, False)])
+def test_stream_k_mxfp8_integers_bit_exact(M, N, K, with_c):
+    prob = inputs.make_problem("mxfp8", M, N, K, seed=M + N, dist="int", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), rows=P.sample_rows(M, 12, seed=4), mode="exact")
+
+
+def test_stream_k_mxfp8_random_tolerance():
+    prob = inputs.make_problem("mxfp8", 128, 1024, 49152, seed=23, dist="normal", with_c=True)
+    P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 12, seed=5), mode="tol")
+
+
 # ------------------------------------------------------------------ argument errors on the GPU
 
 def test_misaligned_output_is_rejected_not_faulted():
