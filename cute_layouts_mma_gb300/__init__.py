@@ -6,6 +6,7 @@ include/tn_gemm.h.  There is no fallback: if the library cannot be built or
 loaded, every call raises.
 
     gemm_f16(A, B, C, D, accum_dtype=GEMM_ACC_F32, stream=None)
+    gemm_f16_noalloc(A, B, C, D, stream=None)
     gemm_block_scaled(A, SFA, B, SFB, C, D, fmt, stream=None)
     gemm_status_string(code), gemm_last_device_error()
 
@@ -30,7 +31,8 @@ GEMM_ACC_F16 = 1
 GEMM_FMT_NVFP4 = 0
 GEMM_FMT_MXFP8 = 1
 
-EXPORTED_SYMBOLS = ("gemm_f16", "gemm_block_scaled", "gemm_status_string", "gemm_last_device_error")
+EXPORTED_SYMBOLS = ("gemm_f16", "gemm_f16_noalloc", "gemm_block_scaled", "gemm_status_string",
+                    "gemm_last_device_error")
 
 
 class GemmError(RuntimeError):
@@ -60,6 +62,8 @@ def lib() -> ctypes.CDLL:
                 i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
                 l.gemm_f16.argtypes = [i64, i64, i64, vp, vp, vp, vp, ci, vp]
                 l.gemm_f16.restype = ci
+                l.gemm_f16_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+                l.gemm_f16_noalloc.restype = ci
                 l.gemm_block_scaled.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, ci, vp]
                 l.gemm_block_scaled.restype = ci
                 l.gemm_status_string.argtypes = [ci]
@@ -116,6 +120,27 @@ def gemm_f16(A, B, C, D, accum_dtype: int = GEMM_ACC_F32, stream=None) -> None:
     with torch.cuda.device(dev):
         _check(lib().gemm_f16(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), int(accum_dtype),
                               _stream(stream)))
+
+
+def gemm_f16_noalloc(A, B, C, D, stream=None) -> None:
+    """gemm_f16 with fp32 accumulation whose scratch is the library's fixed block.
+
+    For callers that must not allocate device memory during the call (the
+    library's own pool included).  Calls that overlap on the GPU share the block
+    and race: keep them ordered on one stream.  Make the first call on a device
+    outside any stream capture (it looks up the block's address).
+    """
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    _need(A, "A", torch.float16, (M, K), dev)
+    _need(B, "B", torch.float16, (N, K), dev)
+    if C is not None:
+        _need(C, "C", torch.float16, (M, N), dev)
+    _need(D, "D", torch.float16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_f16_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _stream(stream)))
 
 
 def gemm_block_scaled(A, SFA, B, SFB, C, D, fmt: int, stream=None) -> None:

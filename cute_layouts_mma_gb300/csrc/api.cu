@@ -141,6 +141,24 @@ gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const voi
     return launch_gemm_f16(M, N, K, A, B, C, D, accum_dtype, stream, sms, dev);
 }
 
+gemm_status_t gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                               void* D, cudaStream_t stream) {
+    using namespace tn;
+    if (!size_ok(M) || !size_ok(N) || !size_ok(K)) return GEMM_ERR_INVALID_ARG;
+    if (A == nullptr || B == nullptr || D == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_ALIGNMENT;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (C != nullptr && !aligned16(C)))
+        return GEMM_ERR_ALIGNMENT;
+    const uint64_t abytes = uint64_t(M) * uint64_t(K) * 2, bbytes = uint64_t(N) * uint64_t(K) * 2;
+    const uint64_t dbytes = uint64_t(M) * uint64_t(N) * 2;
+    if (overlaps(D, dbytes, A, abytes) || overlaps(D, dbytes, B, bbytes) || !c_d_ok(C, D, dbytes))
+        return GEMM_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    gemm_status_t st = device_info(&dev, &sms);
+    if (st != GEMM_OK) return st;
+    return launch_gemm_f16_noalloc(M, N, K, A, B, C, D, stream, sms, dev);
+}
+
 gemm_status_t gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA, const void* B,
                                 const void* SFB, const void* C, void* D, int fmt, cudaStream_t stream) {
     using namespace tn;

@@ -75,6 +75,72 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
                 : run<CfgF16Acc16>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch of gemm_f16_noalloc: one fixed block per device, part of the loaded
+// module, so the call never allocates.  20 MiB holds the stream-K partials and
+// flags of a device with up to 159 SMs (a 152-SM GB300 needs 19.0 MiB).  Every
+// call shares it: calls that overlap on the GPU would overwrite each other's
+// partials and flags.
+constexpr size_t kStaticScratchBytes = size_t(20) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+std::atomic<uintptr_t> g_static_scratch_addr[kMaxDevices];
+
+// Device address of the fixed block on device `dev` (the current device), looked
+// up once per device; null if the lookup fails.
+void* static_scratch(int dev) {
+    uintptr_t a = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+    if (a == 0) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) return nullptr;
+        a = reinterpret_cast<uintptr_t>(ptr);
+        g_static_scratch_addr[dev].store(a, std::memory_order_release);
+    }
+    return reinterpret_cast<void*>(a);
+}
+
+template <class Cfg>
+gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                          cudaStream_t stream, int sms, int dev) {
+    CUtensorMap ta, tb, td, tc;
+    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, 64, Cfg::BM, 128) ||
+        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, 64, Cfg::BN_CTA, 128) ||
+        !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
+                       Cfg::EPI_ROW_BYTES))
+        return GEMM_ERR_CUDA;
+    if (C == nullptr)
+        tc = td;
+    else if (!encode_tma_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, Cfg::EPI_COLS, 32, Cfg::EPI_ROW_BYTES))
+        return GEMM_ERR_CUDA;
+    unsigned int* err = err_word(dev);
+    void* scratch = static_scratch(dev);
+    if (err == nullptr || scratch == nullptr) return GEMM_ERR_CUDA;
+    Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
+    p.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
+    p.num_k_blocks = static_cast<int>((K + 63) / 64);
+    p.C = C;
+    p.D = D;
+    p.err = err;
+    const gemm_status_t st =
+        launch_config_fixed_scratch<Cfg>(ta, tb, td, tc, p, sms, dev, stream, scratch, kStaticScratchBytes);
+    if (st != GEMM_OK) return st;
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                                      void* D, cudaStream_t stream, int sms, int dev) {
+    return M > 128 ? run_noalloc<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                   : run_noalloc<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+}
+
 unsigned int read_clear_error_f16() {
     unsigned int v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_err_f16, sizeof(v)) != cudaSuccess) return 0;

@@ -29,6 +29,11 @@ gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const vo
                                        const void* C, void* D, int fmt, cudaStream_t stream,
                                        int sms, int dev);
 
+// FP16 with fp32 accumulation whose stream-K scratch is a fixed block inside the
+// module (no allocation); arguments are already validated.
+gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                                      const void* C, void* D, cudaStream_t stream, int sms, int dev);
+
 // Read and clear the device error word of each kernel family on the current
 // device (synchronous).  Non-zero means a kernel abandoned its work.
 unsigned int read_clear_error_f16();

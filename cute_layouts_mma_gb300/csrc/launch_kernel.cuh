@@ -116,4 +116,58 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     return e != cudaSuccess ? e : f;
 }
 
+// Same launch, but the stream-K scratch is the caller's fixed block `scratch` of
+// `capacity` bytes (256-byte aligned) instead of a pool allocation: nothing is
+// allocated or freed.  A split launch whose partials and flags would not fit is
+// refused with GEMM_ERR_INVALID_ARG before anything is enqueued.  The block's
+// flags are cleared on `stream` before the kernel; its partials need no clearing
+// (each is written before its flag is raised).
+template <class Cfg>
+gemm_status_t launch_config_fixed_scratch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                                          const CUtensorMap& tc, Params p, int sms, int dev, cudaStream_t stream,
+                                          void* scratch, size_t capacity) {
+    auto kernel = tn_gemm_kernel<Cfg>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    if (Cfg::PAIR == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    int units = LaunchState<Cfg>::max_units[dev].load(std::memory_order_acquire);
+    if (units == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+        units = sms;
+        if (Cfg::PAIR == 2) {
+            cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) return GEMM_ERR_CUDA;
+            units = clusters > 0 ? clusters : sms / 2;
+        }
+        LaunchState<Cfg>::max_units[dev].store(units, std::memory_order_release);
+    }
+    const Schedule sc = choose_schedule<Cfg>(p, units);
+    cfg.gridDim = dim3(sc.units * Cfg::PAIR, 1, 1);
+    p.sk_tiles = sc.sk_tiles;
+    p.sk_total = static_cast<long long>(sc.sk_tiles) * p.num_k_blocks;
+    p.ws = nullptr;
+    p.flags = nullptr;
+    if (sc.sk_tiles != 0) {
+        const size_t pbytes = sk_partial_bytes<Cfg>(sc.units), fbytes = sk_flag_bytes<Cfg>(sc.units);
+        if (scratch == nullptr || pbytes + fbytes > capacity) return GEMM_ERR_INVALID_ARG;
+        p.ws = static_cast<float*>(scratch);
+        p.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(scratch) + pbytes);
+        if (cudaMemsetAsync(p.flags, 0, fbytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, ta, tb, td, tc, p) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 }  // namespace tn

@@ -92,6 +92,41 @@ gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, const voi
                        const void *C, void *D, int accum_dtype, cudaStream_t stream);
 
 /*
+ * FP16 TN GEMM with fp32 accumulation that allocates nothing.
+ *
+ * The pages have no counterpart of this call: it exists for callers that must
+ * not allocate device memory while they run.  Examples are a plugin inside a
+ * host application that owns all device memory and hands out only the buffers
+ * it chose, a serving loop that has reserved nearly all of HBM up front (so
+ * any later allocation may fail), and code whose latency budget cannot absorb
+ * an allocation.  gemm_f16 takes its stream-K scratch from a memory pool; this
+ * call instead uses a fixed 20 MiB block that is part of the library's module
+ * and that every GPU which loads the library holds until the process exits.
+ *
+ *   M, N, K, A, B, C, D, stream   as gemm_f16 (fp32 accumulation); the result
+ *                agrees with gemm_f16's within the fp32 accumulation tolerance
+ *                (on one device the two choose the same schedule).
+ * Scratch limits:
+ *   - The call never calls cudaMalloc, cudaFree or a pool allocator.  Its first
+ *     call on a device looks up the block's device address there (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - A stream-K launch needs 128 KB of fp32 partials per SM it runs on, plus
+ *     flags: 19.0 MiB on a 152-SM GB300.  A launch whose need exceeds the 20 MiB
+ *     block (a device of more than 159 SMs) is refused with
+ *     GEMM_ERR_INVALID_ARG and nothing is enqueued.  Whole-tile launches use no
+ *     scratch.
+ *   - Every call on a device shares the block and it keeps the last call's
+ *     contents: each call clears the flags it uses (an async memset on
+ *     `stream`); partial sums are written before they are read.  Calls that
+ *     overlap on the GPU (e.g. on two streams without ordering between them)
+ *     race on the block and give wrong results; order them on one stream.
+ * Returns as gemm_f16.
+ */
+gemm_status_t gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                               const void *C, void *D, cudaStream_t stream);
+
+/*
  * Block-scaled TN GEMM:
  *   D[m][n] = round_bf16( C[m][n] + sum_k (A[m][k] * SFA[m][k/K_blk])
  *                                         * (B[n][k] * SFB[n][k/K_blk]) ).

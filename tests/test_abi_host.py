@@ -69,6 +69,15 @@ def test_f16_rejections():
     assert _f16(64, 64, 64, C=4 * P + 16) == tg.GEMM_ERR_INVALID_ARG
 
 
+def test_f16_noalloc_rejections():
+    f = lambda M, N, K, A=P, B=2 * P, C=None, D=4 * P: tg.lib().gemm_f16_noalloc(M, N, K, A, B, C, D, None)
+    assert f(0, 8, 8) == tg.GEMM_ERR_INVALID_ARG
+    assert f(8, 8, 8, B=None) == tg.GEMM_ERR_INVALID_ARG
+    assert f(8, 8, 12) == tg.GEMM_ERR_ALIGNMENT
+    assert f(8, 8, 8, D=P + 8) == tg.GEMM_ERR_ALIGNMENT
+    assert f(64, 64, 64, D=2 * P) == tg.GEMM_ERR_INVALID_ARG
+
+
 def test_block_scaled_rejections():
     for fmt in (tg.GEMM_FMT_NVFP4, tg.GEMM_FMT_MXFP8):
         assert _bs(0, 8, 512, fmt) == tg.GEMM_ERR_INVALID_ARG
