@@ -472,6 +472,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_base_slot;
+    // The set-up above touched only this CTA's own shared memory, TMEM and parameters,
+    // so it may overlap the end of the previous launch on the stream (launched with
+    // programmatic stream serialization).  Global memory is touched only after the
+    // previous grid has completed; the next launch may start its own set-up now.
+    griddep_wait();
+    griddep_launch_dependents();
 
     // ------------------------------------------------------------------ TMA issuers
     // role 0: A, 1: B, 2: SFA, 3: SFB.  Each waits for its stage slot to be released

@@ -68,17 +68,17 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
                           int sms, int dev, cudaStream_t stream) {
     auto kernel = tn_gemm_kernel<Cfg>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
+    cfg.attrs = attr;
     if (Cfg::PAIR == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = 2;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
     }
     int units = LaunchState<Cfg>::max_units[dev].load(std::memory_order_acquire);
     if (units == 0) {
@@ -97,6 +97,11 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     }
     const Schedule sc = choose_schedule<Cfg>(p, units);
     cfg.gridDim = dim3(sc.units * Cfg::PAIR, 1, 1);
+    // The kernel's set-up may overlap the previous launch on the stream; it waits
+    // (griddepcontrol.wait) before touching global memory.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
     p.sk_tiles = sc.sk_tiles;
     p.sk_total = static_cast<long long>(sc.sk_tiles) * p.num_k_blocks;
     p.ws = nullptr;
@@ -128,17 +133,17 @@ gemm_status_t launch_config_fixed_scratch(const CUtensorMap& ta, const CUtensorM
                                           void* scratch, size_t capacity) {
     auto kernel = tn_gemm_kernel<Cfg>;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
+    cfg.attrs = attr;
     if (Cfg::PAIR == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = 2;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
     }
     int units = LaunchState<Cfg>::max_units[dev].load(std::memory_order_acquire);
     if (units == 0) {
@@ -156,6 +161,11 @@ gemm_status_t launch_config_fixed_scratch(const CUtensorMap& ta, const CUtensorM
     }
     const Schedule sc = choose_schedule<Cfg>(p, units);
     cfg.gridDim = dim3(sc.units * Cfg::PAIR, 1, 1);
+    // The kernel's set-up may overlap the previous launch on the stream; it waits
+    // (griddepcontrol.wait) before touching global memory.
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
     p.sk_tiles = sc.sk_tiles;
     p.sk_total = static_cast<long long>(sc.sk_tiles) * p.num_k_blocks;
     p.ws = nullptr;

@@ -103,6 +103,13 @@ __device__ __forceinline__ void bulk_wait_group_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: block until every grid this launch
+// depends on has completed and its memory is visible (returns at once when there is
+// none).  griddep_launch_dependents: let the next launch on the stream, if it opted
+// in, be scheduled while this grid still runs.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
