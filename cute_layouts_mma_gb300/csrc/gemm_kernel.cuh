@@ -308,10 +308,9 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 template <int KIND, int COLS, bool kCStaged>
 __device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int lane) {
     constexpr int VECS = COLS / 8;  // 16-byte output vectors per row
-    const int swz = (COLS == 64) ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
     for (int v = 0; v < VECS; ++v) {
-        uint4* slot = reinterpret_cast<uint4*>(buf + lane * (COLS * 2) + ((v ^ swz) * 16));
+        uint4* slot = reinterpret_cast<uint4*>(buf + layout::swizzled_offset(COLS * 2, lane, 16 * v));
         float f[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
@@ -344,7 +343,7 @@ __device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t
         uint32_t R[SET][4];
 #pragma unroll
         for (int c = 0; c < SET; ++c) {
-            const uint8_t* src = (c < 4) ? raw_a + (lane + 32 * c) * 16 : raw_b + (lane + 32 * (c - 4)) * 16;
+            const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * 16 : raw_b + layout::sf_row(lane, c - 4) * 16;
             const uint4 x = *reinterpret_cast<const uint4*>(src);
             R[c][0] = x.x;
             R[c][1] = x.y;
@@ -365,7 +364,7 @@ __device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t
         uint32_t out[SET];
 #pragma unroll
         for (int c = 0; c < SET; ++c) {
-            const uint8_t* src = (c < 4) ? raw_a + (lane + 32 * c) * 16 : raw_b + (lane + 32 * (c - 4)) * 16;
+            const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * 16 : raw_b + layout::sf_row(lane, c - 4) * 16;
             out[c] = reinterpret_cast<const uint32_t*>(src)[word];
         }
         tmem_st_32x32b_x8(taddr, out);

@@ -1,7 +1,9 @@
-// Inline-PTX wrappers for sm_103a: mbarrier, TMA tensor loads, tcgen05 (TMEM
-// allocation, MMA, scale-factor copy, loads) and the shared-memory / instruction
+// Inline-PTX wrappers for sm_103a: mbarrier, TMA tensor loads and stores, tcgen05
+// (TMEM allocation, MMA, loads and stores) and the shared-memory / instruction
 // descriptors the tcgen05 MMA reads.
 #pragma once
+
+#include "layout.cuh"
 
 #include <cstdint>
 #include <cuda.h>  // CUtensorMap
@@ -186,13 +188,6 @@ __device__ __forceinline__ void mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t adesc,
         : "memory");
 }
 
-// Copy a 32-row x 16-byte shared-memory tile into TMEM at `taddr` (32 lanes x 4
-// columns) and replicate it to all four 32-lane partitions (.warpx4).
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own TMEM
 // lane (lane = 32 * (warp % 4) + laneid).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -245,24 +240,7 @@ __device__ __forceinline__ void tmem_st_wait() {
 // "Swizzle Layout").  Stepping K inside the 128-byte row adds bytes to the start
 // address; the tile base is 1024-byte aligned.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // bits 0-13: start address / 16
-    d |= static_cast<uint64_t>(1) << 16;                   // bits 16-29: leading offset (unused)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // bits 32-45: 8-row group stride
-    d |= static_cast<uint64_t>(1) << 46;                   // bits 46-47: descriptor version
-    d |= static_cast<uint64_t>(2) << 61;                   // bits 61-63: 128-byte swizzle
-    return d;
-}
-
-// Shared-memory descriptor of a plain (unswizzled) 32-row x 16-byte tile, rows
-// 16 bytes apart: four 8-row core matrices of 128 bytes each.
-__device__ __forceinline__ uint64_t smem_desc_sf_tile(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128 >> 4) << 16;  // leading offset: next core matrix along K
-    d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride offset: next 8-row core matrix
-    d |= static_cast<uint64_t>(1) << 46;
-    return d;  // layout type 0: no swizzle
+    return layout::umma_smem_desc_kmajor(saddr, 128);
 }
 
 // Instruction descriptor, kind::f16: FP16 A and B, both K-major; D in fp32

@@ -91,6 +91,14 @@ def test_fp16_4096_full_size_sampled_rows():
 
 # ------------------------------------------------------------------ FP16 accumulation
 
+@pytest.mark.parametrize("M,N,K,rows", [(512, 768, 8192, None), (4096, 4096, 8192, 24)])
+def test_fp16_pairs_long_k_whole_tiles(M, N, K, rows):
+    # CTA pairs over whole tiles with more k-blocks than the 4096^3 workload
+    prob = inputs.make_problem("f16", M, N, K, seed=K + M, dist="normal0.1", with_c=True)
+    D = P.run_gpu(prob, accum=0)
+    P.check(prob, D, rows=None if rows is None else P.sample_rows(M, rows, seed=7), mode="tol")
+
+
 def test_fp16acc_integers_bit_exact():
     # every partial sum is an integer of magnitude <= 1024: exact in fp16
     prob = inputs.make_problem("f16", 256, 264, 256, seed=11, dist="int2", with_c=False)
