@@ -1,4 +1,4 @@
-"""CPU oracle for the TN GEMM D = A x B + C (FP16 and block-scaled NVFP4 / MXFP8).
+"""CPU oracle for the TN GEMM D = A x B + C (FP16, BF16, FP8 and block-scaled NVFP4 / MXFP8).
 
 TEST INFRASTRUCTURE ONLY.  This package is the independent checker of the CUDA
 library: only the tests, the package smoke check and the benchmark's CPU-baseline
@@ -65,7 +65,7 @@ def lib() -> ctypes.CDLL:
         l.oracle_f16_to_f64.restype = ctypes.c_double
         l.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         l.oracle_bf16_to_f64.restype = ctypes.c_double
-        for name in ("oracle_e2m1_to_f64", "oracle_e4m3_to_f64", "oracle_e8m0_to_f64"):
+        for name in ("oracle_e2m1_to_f64", "oracle_e4m3_to_f64", "oracle_e5m2_to_f64", "oracle_e8m0_to_f64"):
             getattr(l, name).argtypes = [ctypes.c_uint8]
             getattr(l, name).restype = ctypes.c_double
         l.oracle_f64_to_f16.argtypes = [ctypes.c_double]
@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
         l.oracle_gemm_block_scaled.argtypes = [ctypes.c_int, i64, i64, i64, u8p, u8p, u8p, u8p,
                                                u16p, i64p, i64, u16p, f64p]
         l.oracle_gemm_block_scaled.restype = ctypes.c_int
+        vp = ctypes.c_void_p
+        l.oracle_gemm_dense.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64, i64, vp, vp,
+                                        u16p, i64p, i64, u16p, f64p]
+        l.oracle_gemm_dense.restype = ctypes.c_int
         l.oracle_num_threads.argtypes = []
         l.oracle_num_threads.restype = ctypes.c_int
         _lib = l
@@ -158,6 +162,41 @@ def gemm_block_scaled(fmt: int, A, SFA, B, SFB, C=None, rows=None, exact: bool =
     return (D16, D64) if exact else D16
 
 
+# element formats of gemm_dense
+FP16, BF16, E4M3, E5M2 = 0, 1, 2, 3
+
+
+def _dense_operand(x, fmt: int) -> np.ndarray:
+    return _bits16(x) if fmt in (FP16, BF16) else _bytes(x)
+
+
+def gemm_dense(A, B, C=None, a_fmt: int = BF16, b_fmt: int = BF16, out_fmt: int = BF16, rows=None,
+               exact: bool = False):
+    """D = round_out(C + A @ B^T) for A a_fmt[M][K], B b_fmt[N][K] (TN), fp64 sums.
+
+    Formats: FP16 / BF16 (torch half / bfloat16 tensors or uint16 bit arrays),
+    E4M3 / E5M2 (torch float8 tensors or uint8 code arrays).  C and D are out_fmt
+    (FP16 or BF16) bits.  Returns uint16 bits [rows, N] (plus the fp64 sums if exact).
+    """
+    Ab, Bb = _dense_operand(A, a_fmt), _dense_operand(B, b_fmt)
+    M, K = Ab.shape
+    N, K2 = Bb.shape
+    assert K == K2
+    Cb = None if C is None else _bits16(C)
+    if Cb is not None:
+        assert Cb.shape == (M, N)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nr = M if r is None else len(r)
+    D16 = np.zeros((nr, N), dtype=np.uint16)
+    D64 = np.zeros((nr, N), dtype=np.float64) if exact else None
+    rc = lib().oracle_gemm_dense(a_fmt, b_fmt, out_fmt, M, N, K, Ab.ctypes.data, Bb.ctypes.data,
+                                 _ptr(Cb, ctypes.c_uint16), _ptr(r, ctypes.c_int64), nr,
+                                 _ptr(D16, ctypes.c_uint16), _ptr(D64, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle: unknown element format")
+    return (D16, D64) if exact else D16
+
+
 def f16_to_f64(bits: int) -> float:
     return lib().oracle_f16_to_f64(int(bits))
 
@@ -172,6 +211,10 @@ def e2m1_to_f64(code: int) -> float:
 
 def e4m3_to_f64(code: int) -> float:
     return lib().oracle_e4m3_to_f64(int(code))
+
+
+def e5m2_to_f64(code: int) -> float:
+    return lib().oracle_e5m2_to_f64(code)
 
 
 def e8m0_to_f64(code: int) -> float:

@@ -14,6 +14,11 @@
  *     are M x N.  Every term and the sum are taken in fp64; round() is one
  *     round-to-nearest-even to fp16, applied once at the end.
  *
+ *   Dense, other element types:  D[m][n] = round( C[m][n] + sum_k a[m][k] * b[n][k] )
+ *     the same TN multiply-accumulate (section 1 of the CuTe page) with A and B
+ *     in BF16, FP8 E4M3 or FP8 E5M2 and C / D in fp16 or bf16; every term and
+ *     the sum in fp64, one round-to-nearest-even at the end.
+ *
  *   Block-scaled:  A_real[m][k] = A_low[m][k] * SFA[m][k / K_blk]
  *                  B_real[n][k] = B_low[n][k] * SFB[n][k / K_blk]
  *                  D = C + A_real x B_real  (rounded once to bf16)
@@ -28,8 +33,9 @@
  *   - The element encodings are not defined on the pages; the decoders below
  *     follow the OCP microscaling / FP8 definitions: E2M1 (1 sign, 2 exponent
  *     bits, bias 1, 1 mantissa bit, no Inf/NaN), E4M3 "fn" (bias 7,
- *     subnormals, S.1111.111 is NaN, no Inf, max 448), E8M0 (2^(e-127),
- *     0xFF is NaN).
+ *     subnormals, S.1111.111 is NaN, no Inf, max 448), E5M2 (bias 15, two
+ *     mantissa bits, subnormals, exponent 31 is Inf or NaN as in IEEE 754),
+ *     E8M0 (2^(e-127), 0xFF is NaN).  BF16 is the upper half of an IEEE fp32.
  *   - FP4 packing: element 2j sits in the low nibble of byte j, element 2j+1
  *     in the high nibble (the pages' "lower slot = low 16 bits" packing rule
  *     for two halves in one 32-bit operand, carried over to two nibbles).
@@ -91,6 +97,19 @@ double oracle_e4m3_to_f64(uint8_t code) {
     else
         v = ldexp(1.0 + m / 8.0, e - 7);
     return s ? -v : v;
+}
+
+/* E5M2 from its bit fields: bias 15, 2 mantissa bits, IEEE-style Inf / NaN. */
+double oracle_e5m2_to_f64(uint8_t code) {
+    int sign = code >> 7, exp = (code >> 2) & 0x1f, man = code & 3;
+    double v;
+    if (exp == 31)
+        v = man ? NAN : INFINITY;
+    else if (exp == 0)
+        v = ldexp((double)man / 4.0, -14);
+    else
+        v = ldexp(1.0 + (double)man / 4.0, exp - 15);
+    return sign ? -v : v;
 }
 
 /* E8M0: a pure power of two, 2^(code - 127); 0xFF is NaN. */
@@ -225,6 +244,49 @@ int oracle_gemm_block_scaled(int fmt, int64_t M, int64_t N, int64_t K, const uin
                 D64[i * N + n] = acc;
             if (D16)
                 D16[i * N + n] = oracle_f64_to_bf16(acc);
+        }
+    }
+    return 0;
+}
+
+/* Element formats of oracle_gemm_dense. */
+enum { FMT_FP16 = 0, FMT_BF16 = 1, FMT_E4M3 = 2, FMT_E5M2 = 3 };
+
+static double dense_element(int fmt, const void *X, int64_t idx) {
+    switch (fmt) {
+        case FMT_FP16: return oracle_f16_to_f64(((const uint16_t *)X)[idx]);
+        case FMT_BF16: return oracle_bf16_to_f64(((const uint16_t *)X)[idx]);
+        case FMT_E4M3: return oracle_e4m3_to_f64(((const uint8_t *)X)[idx]);
+        default: return oracle_e5m2_to_f64(((const uint8_t *)X)[idx]);
+    }
+}
+
+/*
+ * Dense TN GEMM for any pair of element formats.  A: a_fmt[M][K], B: b_fmt[N][K]
+ * (fp16 / bf16 as uint16_t bit patterns, E4M3 / E5M2 as bytes); C: out_fmt[M][N]
+ * or NULL; out_fmt 0 = fp16, 1 = bf16.  rows / nrows / D16 / D64 as for
+ * oracle_gemm_f16.  Returns 0, or -1 for an unknown format.
+ */
+int oracle_gemm_dense(int a_fmt, int b_fmt, int out_fmt, int64_t M, int64_t N, int64_t K, const void *A,
+                      const void *B, const uint16_t *C, const int64_t *rows, int64_t nrows, uint16_t *D16,
+                      double *D64) {
+    if (a_fmt < FMT_FP16 || a_fmt > FMT_E5M2 || b_fmt < FMT_FP16 || b_fmt > FMT_E5M2)
+        return -1;
+    if (out_fmt != FMT_FP16 && out_fmt != FMT_BF16)
+        return -1;
+    if (rows == NULL)
+        nrows = M;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = C ? dense_element(out_fmt, C, m * N + n) : 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += dense_element(a_fmt, A, m * K + k) * dense_element(b_fmt, B, n * K + k);
+            if (D64)
+                D64[i * N + n] = acc;
+            if (D16)
+                D16[i * N + n] = out_fmt == FMT_FP16 ? oracle_f64_to_f16(acc) : oracle_f64_to_bf16(acc);
         }
     }
     return 0;

@@ -76,6 +76,14 @@ def test_e4m3_all_codes_vs_torch():
     assert oracle.e4m3_to_f64(0x7E) == 448.0
 
 
+def test_e5m2_all_codes_vs_torch():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).double().numpy()
+    for c in range(256):
+        assert _same(oracle.e5m2_to_f64(c), float(ref[c])), hex(c)
+    assert oracle.e5m2_to_f64(0x7B) == 57344.0 and oracle.e5m2_to_f64(0x7C) == float("inf")
+    assert oracle.e5m2_to_f64(0x01) == 2.0 ** -16  # smallest subnormal
+
+
 def test_e8m0_all_codes_vs_torch():
     ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
     for c in range(256):

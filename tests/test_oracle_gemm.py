@@ -178,3 +178,83 @@ def test_block_scaled_rejects_ragged_k():
     SF = np.zeros((2, 1), np.uint8)
     with pytest.raises(ValueError):
         oracle.gemm_block_scaled(oracle.MXFP8, A, SF, A, SF)
+
+
+# ---- dense GEMM over BF16 / FP8 operands ------------------------------------------
+
+_TORCH = {oracle.FP16: torch.float16, oracle.BF16: torch.bfloat16,
+          oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
+
+
+def _cast(x, fmt):
+    return x.to(_TORCH[fmt])
+
+
+def _exact_dense(A, B, C):
+    """Exact rational sums of the decoded (torch) operand values."""
+    a = [[Fraction(float(x)) for x in row] for row in A.double().tolist()]
+    b = [[Fraction(float(x)) for x in row] for row in B.double().tolist()]
+    c = [[Fraction(float(x)) for x in row] for row in C.double().tolist()] if C is not None else None
+    return [[(c[m][n] if c else 0) + sum(a[m][k] * b[n][k] for k in range(len(a[0])))
+             for n in range(len(b))] for m in range(len(a))]
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt,out_fmt", [(oracle.BF16, oracle.BF16, oracle.BF16),
+                                                 (oracle.E4M3, oracle.E4M3, oracle.BF16),
+                                                 (oracle.E5M2, oracle.E5M2, oracle.BF16),
+                                                 (oracle.E4M3, oracle.E5M2, oracle.FP16)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 7), (6, 4, 16)])
+def test_dense_brute_force_exact_rationals(a_fmt, b_fmt, out_fmt, M, N, K):
+    g = torch.Generator().manual_seed(M * 100 + N * 10 + K + 7 * a_fmt + b_fmt)
+    A = _cast(torch.randn(M, K, generator=g) * 2, a_fmt)
+    B = _cast(torch.randn(N, K, generator=g) * 2, b_fmt)
+    C = _cast(torch.randn(M, N, generator=g), out_fmt)
+    d16, d64 = oracle.gemm_dense(A, B, C, a_fmt, b_fmt, out_fmt, exact=True)
+    ex = _exact_dense(A, B, C)
+    out_t = _TORCH[out_fmt]
+    for m in range(M):
+        for n in range(N):
+            assert Fraction(d64[m, n]) == ex[m][n]  # products of <= 8-bit mantissas sum exactly here
+            want = torch.tensor([float(ex[m][n])], dtype=torch.float64).to(out_t).view(torch.int16).item() & 0xFFFF
+            assert d16[m, n] == want
+
+
+@pytest.mark.parametrize("fmt,lo,hi", [(oracle.BF16, -8, 9), (oracle.E4M3, -8, 9), (oracle.E5M2, -4, 5)])
+def test_dense_small_integers_exact_vs_numpy(fmt, lo, hi):
+    g = torch.Generator().manual_seed(20 + fmt)
+    M, N, K = 48, 40, 136
+    A = torch.randint(lo, hi, (M, K), generator=g).float()
+    B = torch.randint(lo, hi, (N, K), generator=g).float()
+    C = torch.randint(-50, 51, (M, N), generator=g).float()
+    want = np.matmul(A.double().numpy(), B.double().numpy().T) + C.double().numpy()
+    d = oracle.gemm_dense(_cast(A, fmt), _cast(B, fmt), C.bfloat16(), fmt, fmt, oracle.BF16)
+    assert np.array_equal(d, torch.from_numpy(want).bfloat16().view(torch.int16).numpy().view(np.uint16))
+
+
+def test_dense_identity_permutation_and_fp16_agreement():
+    g = torch.Generator().manual_seed(5)
+    n = 32
+    B = torch.randn(n, n, generator=g).to(torch.float8_e4m3fn)
+    I = torch.eye(n).to(torch.float8_e4m3fn)
+    val = lambda bits: oracle.bf16_bits_to_f64_array(bits)  # compares -0 equal to +0
+    # A = I: D[m][n] = B[n][m], exact in bf16 (every E4M3 value is a bf16 value)
+    d = oracle.gemm_dense(I, B, None, oracle.E4M3, oracle.E4M3, oracle.BF16)
+    assert np.array_equal(val(d), B.T.double().numpy())
+    perm = torch.randperm(n, generator=g)
+    P = torch.zeros(n, n).index_put_((torch.arange(n), perm), torch.ones(n)).to(torch.float8_e4m3fn)
+    d = oracle.gemm_dense(P, B, None, oracle.E4M3, oracle.E4M3, oracle.BF16)
+    assert np.array_equal(val(d), B.T.contiguous()[perm].double().numpy())
+    # fp16 operands and fp16 output: the same numbers as the FP16 oracle
+    A16 = torch.randn(9, 20, generator=g).half()
+    B16 = torch.randn(11, 20, generator=g).half()
+    C16 = torch.randn(9, 11, generator=g).half()
+    assert np.array_equal(oracle.gemm_dense(A16, B16, C16, oracle.FP16, oracle.FP16, oracle.FP16),
+                          oracle.gemm_f16(A16, B16, C16))
+
+
+def test_dense_rejects_unknown_format():
+    A = np.zeros((2, 4), dtype=np.uint8)
+    with pytest.raises(ValueError):
+        oracle.gemm_dense(A, A, None, 7, oracle.E4M3, oracle.BF16)
+    with pytest.raises(ValueError):
+        oracle.gemm_dense(A, A, None, oracle.E4M3, oracle.E4M3, oracle.E4M3)
