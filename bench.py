@@ -31,10 +31,13 @@ sys.path.insert(0, ROOT)
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense tensor rates relative to bf16 (2.25 PF): fp8 4.5 PF, fp4 13.5 PF
-NOMINAL_RATIO = {"f16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
+NOMINAL_RATIO = {"f16": 1.0, "bf16": 1.0, "mxfp8": 2.0, "fp8e4m3": 2.0, "fp8e5m2": 2.0, "nvfp4": 6.0}
+DTYPE_NAME = {"nvfp4": "nvfp4 (e2m1+e4m3/16)", "mxfp8": "mxfp8 (e4m3+e8m0/32)", "bf16": "bf16",
+              "fp8e4m3": "fp8 e4m3", "fp8e5m2": "fp8 e5m2"}
 METRIC = "GEMM TFLOPS (FP16 TN, NVFP4/MXFP8 block-scaled) and % of dense tensor peak"
 KERNEL_SOURCES = ["cute_layouts_mma_gb300/csrc/gemm_kernel.cuh", "cute_layouts_mma_gb300/csrc/ptx.cuh",
-                  "cute_layouts_mma_gb300/csrc/gemm_f16.cu", "cute_layouts_mma_gb300/csrc/gemm_bs.cu"]
+                  "cute_layouts_mma_gb300/csrc/layout.cuh", "cute_layouts_mma_gb300/csrc/gemm_f16.cu",
+                  "cute_layouts_mma_gb300/csrc/gemm_bs.cu", "cute_layouts_mma_gb300/csrc/gemm_dense.cu"]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -78,8 +81,11 @@ def recorded_traffic(workload: str):
 
 def workload_bytes(w) -> int:
     """Algorithmic HBM bytes of one launch: read A, B, scales, C once; write D once."""
-    if w.kind == "f16":
+    if w.kind in ("f16", "bf16"):
         ab = 2 * (w.M + w.N) * w.K
+        sf = 0
+    elif w.kind in ("fp8e4m3", "fp8e5m2"):
+        ab = (w.M + w.N) * w.K
         sf = 0
     elif w.kind == "nvfp4":
         ab = (w.M + w.N) * w.K // 2
@@ -157,19 +163,24 @@ class GemmRunner:
         self.w, self.dev, self.tg = w, dev, tg
         base = inputs.make_problem(w.kind, w.M, w.N, w.K, w.seed, w.dist, w.with_c)
         self.host = base
-        out_dtype = torch.float16 if w.kind == "f16" else torch.bfloat16
+        out_dtype = torch.float16 if w.kind == "f16" else torch.bfloat16  # bf16 C / D otherwise
         first = {k: (base[k].to(dev) if base.get(k) is not None else None) for k in ("A", "B", "C", "SFA", "SFB")}
         self.sets = []
         for i in range(sets):
             s = {k: (v if i == 0 or v is None else v.clone()) for k, v in first.items()}
             s["D"] = torch.empty(w.M, w.N, dtype=out_dtype, device=dev)
             self.sets.append(s)
-        self.fmt = tg.GEMM_FMT_NVFP4 if w.kind == "nvfp4" else tg.GEMM_FMT_MXFP8
+        self.fmt = {"nvfp4": tg.GEMM_FMT_NVFP4, "mxfp8": tg.GEMM_FMT_MXFP8, "fp8e4m3": tg.GEMM_FP8_E4M3,
+                    "fp8e5m2": tg.GEMM_FP8_E5M2}.get(w.kind)
 
     def launch(self, i: int, stream=None):
         s = self.sets[i % len(self.sets)]
         if self.w.kind == "f16":
             self.tg.gemm_f16(s["A"], s["B"], s["C"], s["D"], self.w.accum, stream)
+        elif self.w.kind == "bf16":
+            self.tg.gemm_bf16(s["A"], s["B"], s["C"], s["D"], stream)
+        elif self.w.kind in ("fp8e4m3", "fp8e5m2"):
+            self.tg.gemm_fp8(s["A"], s["B"], s["C"], s["D"], self.fmt, stream)
         else:
             self.tg.gemm_block_scaled(s["A"], s["SFA"], s["B"], s["SFB"], s["C"], s["D"], self.fmt, stream)
 
@@ -224,8 +235,8 @@ def roofline(w, ms_per_launch, peaks, peak_src):
         achieved = w.flops / (ms_per_launch * 1e-3) / 1e12
     return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-            "peak_source": peak_src + (" (bf16 x nominal dtype ratio)" if w.kind == "nvfp4" or
-                                       (w.kind == "mxfp8" and bound == "tensor") else ""),
+            "peak_source": peak_src + (" (bf16 x nominal dtype ratio)"
+                                       if bound == "tensor" and NOMINAL_RATIO[w.kind] != 1.0 else ""),
             "algorithmic_bytes": workload_bytes(w), "algorithmic_flops": w.flops}
 
 
@@ -254,6 +265,19 @@ def e2e_measure(runner, steps: int, stream):
     return ms, h2d, d2h
 
 
+def oracle_rows(w, p, rows):
+    """The oracle's result for the given rows of workload w's problem p."""
+    import oracle
+    if w.kind == "f16":
+        return oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows)
+    dense = {"bf16": oracle.BF16, "fp8e4m3": oracle.E4M3, "fp8e5m2": oracle.E5M2}
+    if w.kind in dense:
+        f = dense[w.kind]
+        return oracle.gemm_dense(p["A"], p["B"], p.get("C"), f, f, oracle.BF16, rows=rows)
+    fmt = oracle.NVFP4 if w.kind == "nvfp4" else oracle.MXFP8
+    return oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows)
+
+
 def cpu_baseline(w, budget_s: float):
     """The oracle, as it stands, on a row sample of the workload; TFLOP/s."""
     import numpy as np
@@ -263,11 +287,7 @@ def cpu_baseline(w, budget_s: float):
 
     def run(rows):
         t0 = time.perf_counter()
-        if w.kind == "f16":
-            oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows)
-        else:
-            fmt = oracle.NVFP4 if w.kind == "nvfp4" else oracle.MXFP8
-            oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows)
+        oracle_rows(w, p, rows)
         return time.perf_counter() - t0
 
     threads = oracle.num_threads()
@@ -347,8 +367,7 @@ def gpu_arm(args):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {"f16": "f16" if w.accum == 0 else "f16 (f16 accumulate)", "nvfp4": "nvfp4 (e2m1+e4m3/16)",
-                  "mxfp8": "mxfp8 (e4m3+e8m0/32)"}[w.kind],
+        "dtype": ("f16" if w.accum == 0 else "f16 (f16 accumulate)") if w.kind == "f16" else DTYPE_NAME[w.kind],
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "with_c": w.with_c,
                    "accum": "f32" if w.accum == 0 else "f16",
@@ -402,11 +421,7 @@ def reference_arm(args):
     threads = oracle.num_threads()
 
     def run(rows):
-        if w.kind == "f16":
-            oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows)
-        else:
-            fmt = oracle.NVFP4 if w.kind == "nvfp4" else oracle.MXFP8
-            oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows)
+        oracle_rows(w, p, rows)
 
     probe = list(range(min(w.M, threads)))
     t0 = time.perf_counter()

@@ -7,6 +7,8 @@ loaded, every call raises.
 
     gemm_f16(A, B, C, D, accum_dtype=GEMM_ACC_F32, stream=None)
     gemm_f16_noalloc(A, B, C, D, stream=None)
+    gemm_bf16(A, B, C, D, stream=None)
+    gemm_fp8(A, B, C, D, fmt, stream=None)
     gemm_block_scaled(A, SFA, B, SFB, C, D, fmt, stream=None)
     gemm_status_string(code), gemm_last_device_error()
 
@@ -30,9 +32,11 @@ GEMM_ACC_F32 = 0
 GEMM_ACC_F16 = 1
 GEMM_FMT_NVFP4 = 0
 GEMM_FMT_MXFP8 = 1
+GEMM_FP8_E4M3 = 0
+GEMM_FP8_E5M2 = 1
 
-EXPORTED_SYMBOLS = ("gemm_f16", "gemm_f16_noalloc", "gemm_block_scaled", "gemm_status_string",
-                    "gemm_last_device_error")
+EXPORTED_SYMBOLS = ("gemm_f16", "gemm_f16_noalloc", "gemm_bf16", "gemm_fp8", "gemm_block_scaled",
+                    "gemm_status_string", "gemm_last_device_error")
 
 
 class GemmError(RuntimeError):
@@ -64,6 +68,10 @@ def lib() -> ctypes.CDLL:
                 l.gemm_f16.restype = ci
                 l.gemm_f16_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
                 l.gemm_f16_noalloc.restype = ci
+                l.gemm_bf16.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+                l.gemm_bf16.restype = ci
+                l.gemm_fp8.argtypes = [i64, i64, i64, vp, vp, vp, vp, ci, vp]
+                l.gemm_fp8.restype = ci
                 l.gemm_block_scaled.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, ci, vp]
                 l.gemm_block_scaled.restype = ci
                 l.gemm_status_string.argtypes = [ci]
@@ -141,6 +149,41 @@ def gemm_f16_noalloc(A, B, C, D, stream=None) -> None:
     _need(D, "D", torch.float16, (M, N), dev)
     with torch.cuda.device(dev):
         _check(lib().gemm_f16_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _stream(stream)))
+
+
+def gemm_bf16(A, B, C, D, stream=None) -> None:
+    """D = A @ B^T + C with A bf16[M,K], B bf16[N,K], C bf16[M,N] or None, D bf16[M,N]."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    _need(A, "A", torch.bfloat16, (M, K), dev)
+    _need(B, "B", torch.bfloat16, (N, K), dev)
+    if C is not None:
+        _need(C, "C", torch.bfloat16, (M, N), dev)
+    _need(D, "D", torch.bfloat16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _stream(stream)))
+
+
+def gemm_fp8(A, B, C, D, fmt: int, stream=None) -> None:
+    """D = A @ B^T + C for FP8 A[M,K], B[N,K] (uint8 codes or float8 tensors of the
+    format), C bf16[M,N] or None, D bf16[M,N]; fmt GEMM_FP8_E4M3 or GEMM_FP8_E5M2."""
+    import torch
+    if fmt not in (GEMM_FP8_E4M3, GEMM_FP8_E5M2):
+        raise ValueError("fmt must be GEMM_FP8_E4M3 or GEMM_FP8_E5M2")
+    as_u8 = lambda t: t.view(torch.uint8) if t.dtype != torch.uint8 and t.element_size() == 1 else t
+    A, B = as_u8(A), as_u8(B)
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    _need(A, "A", torch.uint8, (M, K), dev)
+    _need(B, "B", torch.uint8, (N, K), dev)
+    if C is not None:
+        _need(C, "C", torch.bfloat16, (M, N), dev)
+    _need(D, "D", torch.bfloat16, (M, N), dev)
+    with torch.cuda.device(dev):
+        _check(lib().gemm_fp8(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(D), int(fmt), _stream(stream)))
 
 
 def gemm_block_scaled(A, SFA, B, SFB, C, D, fmt: int, stream=None) -> None:

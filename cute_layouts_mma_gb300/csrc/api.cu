@@ -159,6 +159,45 @@ gemm_status_t gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, c
     return launch_gemm_f16_noalloc(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
+// Checks shared by the BF16 and FP8 calls: elem_bytes per operand element, bf16 C / D.
+static gemm_status_t check_dense(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                                 void* D, int elem_bytes) {
+    using namespace tn;
+    if (!size_ok(M) || !size_ok(N) || !size_ok(K)) return GEMM_ERR_INVALID_ARG;
+    if (A == nullptr || B == nullptr || D == nullptr) return GEMM_ERR_INVALID_ARG;
+    if ((K * elem_bytes) % 16 != 0 || N % 8 != 0) return GEMM_ERR_ALIGNMENT;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (C != nullptr && !aligned16(C)))
+        return GEMM_ERR_ALIGNMENT;
+    const uint64_t abytes = uint64_t(M) * uint64_t(K) * elem_bytes, bbytes = uint64_t(N) * uint64_t(K) * elem_bytes;
+    const uint64_t dbytes = uint64_t(M) * uint64_t(N) * 2;
+    if (overlaps(D, dbytes, A, abytes) || overlaps(D, dbytes, B, bbytes) || !c_d_ok(C, D, dbytes))
+        return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                        cudaStream_t stream) {
+    using namespace tn;
+    gemm_status_t st = check_dense(M, N, K, A, B, C, D, 2);
+    if (st != GEMM_OK) return st;
+    int dev = 0, sms = 0;
+    st = device_info(&dev, &sms);
+    if (st != GEMM_OK) return st;
+    return launch_gemm_bf16(M, N, K, A, B, C, D, stream, sms, dev);
+}
+
+gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                       int fmt, cudaStream_t stream) {
+    using namespace tn;
+    if (fmt != GEMM_FP8_E4M3 && fmt != GEMM_FP8_E5M2) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = check_dense(M, N, K, A, B, C, D, 1);
+    if (st != GEMM_OK) return st;
+    int dev = 0, sms = 0;
+    st = device_info(&dev, &sms);
+    if (st != GEMM_OK) return st;
+    return launch_gemm_fp8(M, N, K, A, B, C, D, fmt, stream, sms, dev);
+}
+
 gemm_status_t gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA, const void* B,
                                 const void* SFB, const void* C, void* D, int fmt, cudaStream_t stream) {
     using namespace tn;
@@ -202,8 +241,9 @@ gemm_status_t gemm_last_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
     const unsigned int a = tn::read_clear_error_f16();
     const unsigned int b = tn::read_clear_error_block_scaled();
+    const unsigned int c = tn::read_clear_error_dense();
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
-    return (a | b) ? GEMM_ERR_TIMEOUT : GEMM_OK;
+    return (a | b | c) ? GEMM_ERR_TIMEOUT : GEMM_OK;
 }
 
 }  // extern "C"

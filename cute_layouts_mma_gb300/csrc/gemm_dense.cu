@@ -1,0 +1,96 @@
+// BF16 and unscaled FP8 TN GEMM launchers (tcgen05 kind::f16 with BF16 operands,
+// kind::f8f6f4 with E4M3 or E5M2 operands; fp32 accumulation, bf16 C and D).
+#include <atomic>
+
+#include "launch_kernel.cuh"
+
+namespace tn {
+
+// The same tiles as FP16: CTA pairs of 256 x 256 for M > 128, single CTAs of
+// 128 x 256 otherwise.  A stage holds 128 bytes of K per row: 64 BF16 or 128 FP8
+// elements.
+using CfgBf16Pair = Config<KIND_BF16, 256, 6, 2, 64, 2, 2>;
+using CfgBf16 = Config<KIND_BF16, 256, 4, 2, 64, 2, 1>;
+using CfgE4m3Pair = Config<KIND_FP8_E4M3, 256, 6, 2, 64, 2, 2>;
+using CfgE4m3 = Config<KIND_FP8_E4M3, 256, 4, 2, 64, 2, 1>;
+using CfgE5m2Pair = Config<KIND_FP8_E5M2, 256, 6, 2, 64, 2, 2>;
+using CfgE5m2 = Config<KIND_FP8_E5M2, 256, 4, 2, 64, 2, 1>;
+
+// Device-side record of an abandoned launch (a bounded wait ran out).
+static __device__ unsigned int g_err_dense;
+
+namespace {
+
+std::atomic<uintptr_t> g_err_addr[kMaxDevices];
+
+unsigned int* err_word(int dev) {
+    uintptr_t a = g_err_addr[dev].load(std::memory_order_acquire);
+    if (a == 0) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_err_dense) != cudaSuccess) return nullptr;
+        a = reinterpret_cast<uintptr_t>(ptr);
+        g_err_addr[dev].store(a, std::memory_order_release);
+    }
+    return reinterpret_cast<unsigned int*>(a);
+}
+
+template <class Cfg>
+gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                  cudaStream_t stream, int sms, int dev) {
+    constexpr bool k16 = operands_16bit(Cfg::KIND);
+    const CUtensorMapDataType in_type = k16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t row_bytes = static_cast<uint64_t>(K) * (k16 ? 2 : 1);
+    CUtensorMap ta, tb, td, tc;
+    // A [M][K], 128-row boxes; B [N][K], BN/PAIR-row boxes; 128 bytes of K per box
+    // (64 BF16 or 128 FP8 elements).  D, C: bf16 [M][N] in 32-row x EPI_COLS boxes.
+    if (!encode_tma_2d(&ta, in_type, A, K, M, row_bytes, Cfg::kKCoordPerStage, Cfg::BM, 128) ||
+        !encode_tma_2d(&tb, in_type, B, K, N, row_bytes, Cfg::kKCoordPerStage, Cfg::BN_CTA, 128) ||
+        !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
+                       Cfg::EPI_ROW_BYTES))
+        return GEMM_ERR_CUDA;
+    if (C == nullptr)
+        tc = td;
+    else if (!encode_tma_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, N * 2, Cfg::EPI_COLS, 32,
+                            Cfg::EPI_ROW_BYTES))
+        return GEMM_ERR_CUDA;
+    unsigned int* err = err_word(dev);
+    if (err == nullptr) return GEMM_ERR_CUDA;
+    Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
+    p.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
+    p.num_k_blocks = static_cast<int>((K + Cfg::kKCoordPerStage - 1) / Cfg::kKCoordPerStage);
+    p.C = C;
+    p.D = D;
+    p.err = err;
+    if (launch_config<Cfg>(ta, tb, ta, tb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+gemm_status_t launch_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                               void* D, cudaStream_t stream, int sms, int dev) {
+    return M > 128 ? run<CfgBf16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                   : run<CfgBf16>(M, N, K, A, B, C, D, stream, sms, dev);
+}
+
+gemm_status_t launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                              void* D, int fmt, cudaStream_t stream, int sms, int dev) {
+    if (fmt == GEMM_FP8_E4M3)
+        return M > 128 ? run<CfgE4m3Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                       : run<CfgE4m3>(M, N, K, A, B, C, D, stream, sms, dev);
+    return M > 128 ? run<CfgE5m2Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                   : run<CfgE5m2>(M, N, K, A, B, C, D, stream, sms, dev);
+}
+
+unsigned int read_clear_error_dense() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_dense, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_err_dense, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace tn

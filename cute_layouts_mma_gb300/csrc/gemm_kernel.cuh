@@ -49,7 +49,24 @@
 
 namespace tn {
 
-enum Kind : int { KIND_F16_ACC32 = 0, KIND_F16_ACC16 = 1, KIND_NVFP4 = 2, KIND_MXFP8 = 3 };
+enum Kind : int {
+    KIND_F16_ACC32 = 0,  // FP16 operands, fp32 accumulation, fp16 C / D
+    KIND_F16_ACC16 = 1,  // FP16 operands, fp16 accumulation, fp16 C / D
+    KIND_NVFP4 = 2,      // block-scaled E2M1 (E4M3 scale per 16), bf16 C / D
+    KIND_MXFP8 = 3,      // block-scaled E4M3 (E8M0 scale per 32), bf16 C / D
+    KIND_BF16 = 4,       // BF16 operands, fp32 accumulation, bf16 C / D
+    KIND_FP8_E4M3 = 5,   // unscaled E4M3 operands, fp32 accumulation, bf16 C / D
+    KIND_FP8_E5M2 = 6    // unscaled E5M2 operands, fp32 accumulation, bf16 C / D
+};
+
+// C and D are fp16 for the FP16 kinds and bf16 for every other kind.
+__host__ __device__ constexpr bool out_is_bf16(int kind) { return kind != KIND_F16_ACC32 && kind != KIND_F16_ACC16; }
+// Two-byte operands (64 elements per 128-byte row slice) or one-byte ones (128).
+__host__ __device__ constexpr bool operands_16bit(int kind) {
+    return kind == KIND_F16_ACC32 || kind == KIND_F16_ACC16 || kind == KIND_BF16;
+}
+// MMAs without scale factors: kind::f16 (FP16, BF16) or kind::f8f6f4 (FP8).
+__host__ __device__ constexpr bool is_dense(int kind) { return kind != KIND_NVFP4 && kind != KIND_MXFP8; }
 
 // Upper bound on any single pipeline wait; legitimate waits are microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -155,7 +172,7 @@ struct Config {
     static constexpr int THREADS = EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256);
     static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
-    static constexpr int kKCoordPerStage = (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) ? 64 : 128;
+    static constexpr int kKCoordPerStage = operands_16bit(KIND) ? 64 : 128;
 
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = BN_CTA * 128;
@@ -271,7 +288,7 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        if constexpr (KIND == KIND_NVFP4 || KIND == KIND_MXFP8) {
+        if constexpr (out_is_bf16(KIND)) {
             f[2 * i] = __uint_as_float(w[i] << 16);
             f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         } else {
@@ -288,7 +305,7 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        if constexpr (KIND == KIND_NVFP4 || KIND == KIND_MXFP8) {
+        if constexpr (out_is_bf16(KIND)) {
             const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
             w[i] = *reinterpret_cast<const uint32_t*>(&b);
         } else {
@@ -617,14 +634,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc_fence_after_sync();
                     const uint64_t adesc = adesc0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
                     const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s * (Cfg::B_BYTES >> 4));
-                    if constexpr (KIND == KIND_F16_ACC32 || KIND == KIND_F16_ACC16) {
-                        constexpr uint32_t idesc = idesc_f16(kM, BN, KIND == KIND_F16_ACC32);
+                    if constexpr (is_dense(KIND)) {
+                        // 4 MMAs of 32 bytes of K: 16 elements (kind::f16) or 32 (kind::f8f6f4)
+                        constexpr uint32_t idesc =
+                            idesc_dense(kM, BN, KIND != KIND_F16_ACC16,
+                                        (KIND == KIND_BF16 || KIND == KIND_FP8_E5M2) ? 1u : 0u);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            if constexpr (kPair)
-                                mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
-                            else
-                                mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                            if constexpr (operands_16bit(KIND)) {
+                                if constexpr (kPair)
+                                    mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                                else
+                                    mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                            } else {
+                                if constexpr (kPair)
+                                    mma_f8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                                else
+                                    mma_f8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                            }
                         }
                     } else {
                         const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);

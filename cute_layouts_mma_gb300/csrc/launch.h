@@ -34,10 +34,16 @@ gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const vo
 gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                                       const void* C, void* D, cudaStream_t stream, int sms, int dev);
 
+gemm_status_t launch_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                               const void* C, void* D, cudaStream_t stream, int sms, int dev);
+gemm_status_t launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                              const void* C, void* D, int fmt, cudaStream_t stream, int sms, int dev);
+
 // Read and clear the device error word of each kernel family on the current
 // device (synchronous).  Non-zero means a kernel abandoned its work.
 unsigned int read_clear_error_f16();
 unsigned int read_clear_error_block_scaled();
+unsigned int read_clear_error_dense();
 
 constexpr int kMaxDevices = 64;
 

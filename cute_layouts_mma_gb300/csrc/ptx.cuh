@@ -162,6 +162,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 
+// Dense FP8 MMA without scale factors (kind::f8f6f4): 32 bytes of K per instruction.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Block-scaled MMA, FP8 operands, one scale per 32 K (scale_vec::1X).
 __device__ __forceinline__ void mma_mxf8f6f4_1x(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                 uint32_t idesc, uint32_t sfa_tmem,
@@ -243,12 +254,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return layout::umma_smem_desc_kmajor(saddr, 128);
 }
 
-// Instruction descriptor, kind::f16: FP16 A and B, both K-major; D in fp32
-// (d_f32) or fp16; M x N tile.
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool d_f32) {
+// Instruction descriptor of the dense kinds, both operands K-major, M x N tile,
+// D in fp32 (d_f32) or fp16.  ab_format is the operand type code of the kind:
+// kind::f16 0 = F16, 1 = BF16; kind::f8f6f4 0 = E4M3, 1 = E5M2 (A and B alike).
+__host__ __device__ constexpr uint32_t idesc_dense(int m, int n, bool d_f32, uint32_t ab_format) {
     return (d_f32 ? 1u : 0u) << 4          // D format: 0 = F16, 1 = F32
-           | 0u << 7                       // A format: F16
-           | 0u << 10                      // B format: F16
+           | ab_format << 7                // A format
+           | ab_format << 10               // B format
            | 0u << 15 | 0u << 16           // A, B K-major
            | static_cast<uint32_t>(n >> 3) << 17
            | static_cast<uint32_t>(m >> 4) << 24;
@@ -361,6 +373,16 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, ui
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

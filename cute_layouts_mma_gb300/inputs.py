@@ -18,6 +18,10 @@ Workloads (name -> recipe):
   mxfp8_128x16384     M=128, N=16384, K=8192, E4M3 = RNE(clip(N(0,1), +-448)),
                       E8M0 exponents 127+U{-4..4}, C ~ N(0,1) bf16,
                       fp32 accumulation, bf16 D.                           seed 4
+  bf16_4096           M=N=K=4096, A,B ~ N(0,1)*0.1 as bf16, C ~ N(0,1) bf16,
+                      fp32 accumulation, bf16 D.                           seed 5
+  fp8e4m3_8192        M=N=K=8192, A,B = E4M3 RNE(clip(N(0,1), +-448)), no
+                      scales, C absent, fp32 accumulation, bf16 D.         seed 6
 """
 from __future__ import annotations
 
@@ -29,12 +33,16 @@ import torch
 KIND_F16 = "f16"
 KIND_NVFP4 = "nvfp4"
 KIND_MXFP8 = "mxfp8"
+KIND_BF16 = "bf16"
+KIND_FP8_E4M3 = "fp8e4m3"
+KIND_FP8_E5M2 = "fp8e5m2"
+FP8_KINDS = (KIND_FP8_E4M3, KIND_FP8_E5M2)
 
 
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str          # "f16", "nvfp4" or "mxfp8"
+    kind: str          # "f16", "nvfp4", "mxfp8", "bf16", "fp8e4m3" or "fp8e5m2"
     M: int
     N: int
     K: int
@@ -55,6 +63,8 @@ WORKLOADS = {
         Workload("fp16acc_8192x1024", KIND_F16, 8192, 8192, 1024, "uniform0.5", False, 1, 2),
         Workload("nvfp4_8192", KIND_NVFP4, 8192, 8192, 8192, "codes", False, 0, 3),
         Workload("mxfp8_128x16384", KIND_MXFP8, 128, 16384, 8192, "normal", True, 0, 4),
+        Workload("bf16_4096", KIND_BF16, 4096, 4096, 4096, "normal0.1", True, 0, 5),
+        Workload("fp8e4m3_8192", KIND_FP8_E4M3, 8192, 8192, 8192, "normal", False, 0, 6),
     ]
 }
 
@@ -63,6 +73,10 @@ def make_problem(kind: str, M: int, N: int, K: int, seed: int, dist: str = "defa
                  with_c: bool = True) -> dict:
     """Random operands for one GEMM, as CPU tensors.
 
+    bf16:  as f16 with bfloat16 A, B, C ("int2" or "normal0.1").
+    fp8e4m3 / fp8e5m2: A uint8[M,K], B uint8[N,K] FP8 codes (torch's RNE cast of
+           clip(N(0,1)) to the format; "int": integers -4..4), C bf16 ~ N(0,1)
+           ("int": integers -8..8) or None.
     f16:   A half[M,K], B half[N,K], C half[M,N] or None.  dist: "int2" (integers
            -2..2), "normal0.1" (N(0,1)*0.1), "uniform0.5" (U[-0.5,0.5]), "default"
            (= normal0.1).  C ~ N(0,1) when present ("int2": integers -50..50).
@@ -77,6 +91,29 @@ def make_problem(kind: str, M: int, N: int, K: int, seed: int, dist: str = "defa
     """
     g = torch.Generator().manual_seed(seed)
     out: dict = {"kind": kind, "M": M, "N": N, "K": K}
+    if kind == KIND_BF16:
+        if dist == "int2":
+            A = torch.randint(-2, 3, (M, K), generator=g).to(torch.bfloat16)
+            B = torch.randint(-2, 3, (N, K), generator=g).to(torch.bfloat16)
+            C = torch.randint(-50, 51, (M, N), generator=g).to(torch.bfloat16) if with_c else None
+        else:
+            A = (torch.randn(M, K, generator=g) * 0.1).to(torch.bfloat16)
+            B = (torch.randn(N, K, generator=g) * 0.1).to(torch.bfloat16)
+            C = torch.randn(M, N, generator=g).to(torch.bfloat16) if with_c else None
+        out.update(A=A, B=B, C=C)
+        return out
+    if kind in FP8_KINDS:
+        dt, lim = (torch.float8_e4m3fn, 448.0) if kind == KIND_FP8_E4M3 else (torch.float8_e5m2, 57344.0)
+        if dist == "int":
+            A = torch.randint(-4, 5, (M, K), generator=g).float().to(dt).view(torch.uint8)
+            B = torch.randint(-4, 5, (N, K), generator=g).float().to(dt).view(torch.uint8)
+            C = torch.randint(-8, 9, (M, N), generator=g).float().to(torch.bfloat16) if with_c else None
+        else:
+            A = torch.randn(M, K, generator=g).clamp(-lim, lim).to(dt).view(torch.uint8)
+            B = torch.randn(N, K, generator=g).clamp(-lim, lim).to(dt).view(torch.uint8)
+            C = torch.randn(M, N, generator=g).to(torch.bfloat16) if with_c else None
+        out.update(A=A, B=B, C=C)
+        return out
     if kind == KIND_F16:
         if dist == "int2":
             A = torch.randint(-2, 3, (M, K), generator=g).to(torch.float16)

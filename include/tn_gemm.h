@@ -72,6 +72,7 @@ typedef enum {
 
 enum { GEMM_ACC_F32 = 0, GEMM_ACC_F16 = 1 };   /* accum_dtype of gemm_f16        */
 enum { GEMM_FMT_NVFP4 = 0, GEMM_FMT_MXFP8 = 1 }; /* fmt of gemm_block_scaled      */
+enum { GEMM_FP8_E4M3 = 0, GEMM_FP8_E5M2 = 1 };   /* fmt of gemm_fp8               */
 
 /*
  * FP16 TN GEMM:  D[m][n] = round_fp16( C[m][n] + sum_k A[m][k] * B[n][k] ).
@@ -90,6 +91,41 @@ enum { GEMM_FMT_NVFP4 = 0, GEMM_FMT_MXFP8 = 1 }; /* fmt of gemm_block_scaled    
  */
 gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
                        const void *C, void *D, int accum_dtype, cudaStream_t stream);
+
+/*
+ * BF16 TN GEMM:  D[m][n] = round_bf16( C[m][n] + sum_k A[m][k] * B[n][k] ).
+ *
+ * The same TN multiply-accumulate as gemm_f16 ("CuTe 中 A、B 如何加载到 MMA 寄存器",
+ * section 1) with BF16 operands; products summed in fp32 by the tensor cores
+ * (kind::f16 with BF16 inputs), C added in fp32, one RNE rounding to bf16.
+ *
+ *   M, N, K      each >= 1 and < 2^31; K % 8 == 0 and N % 8 == 0.
+ *   A            bf16[M][K], K contiguous.   B  bf16[N][K], K contiguous.
+ *   C            bf16[M][N] or NULL (zero).  D  bf16[M][N], written; may equal C.
+ *   stream       cudaStream_t the kernel is launched on.
+ * Returns GEMM_OK once the kernel is enqueued, else the first failed check.
+ */
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                        const void *C, void *D, cudaStream_t stream);
+
+/*
+ * FP8 TN GEMM without scale factors:
+ *   D[m][n] = round_bf16( C[m][n] + sum_k decode(A[m][k]) * decode(B[n][k]) ).
+ *
+ * The TN multiply-accumulate of section 1 of the CuTe page with both operands
+ * in the same FP8 format (kind::f8f6f4): GEMM_FP8_E4M3 (bias 7, max 448,
+ * S.1111.111 NaN) or GEMM_FP8_E5M2 (bias 15, max 57344, IEEE Inf / NaN); the
+ * same E4M3 data as the MXFP8 form of gemm_block_scaled with every scale 1.
+ * Products summed in fp32, C added in fp32, one RNE rounding to bf16.
+ *
+ *   M, N, K      each >= 1 and < 2^31; K % 16 == 0 and N % 8 == 0.
+ *   A            u8[M][K] FP8 codes, K contiguous.   B  u8[N][K], K contiguous.
+ *   C            bf16[M][N] or NULL (zero).           D  bf16[M][N]; may equal C.
+ *   fmt          GEMM_FP8_E4M3 or GEMM_FP8_E5M2 (A and B alike).
+ * Returns GEMM_OK once the kernel is enqueued, else the first failed check.
+ */
+gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                       const void *C, void *D, int fmt, cudaStream_t stream);
 
 /*
  * FP16 TN GEMM with fp32 accumulation that allocates nothing.

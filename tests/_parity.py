@@ -33,6 +33,13 @@ def run_gpu(prob: dict, dev=None, accum: int = 0, D=None, stream=None):
     if prob["kind"] == "f16":
         D = torch.empty(M, N, dtype=torch.float16, device=dev) if D is None else D
         tg.gemm_f16(g["A"], g["B"], g.get("C"), D, accum, stream)
+    elif prob["kind"] == "bf16":
+        D = torch.empty(M, N, dtype=torch.bfloat16, device=dev) if D is None else D
+        tg.gemm_bf16(g["A"], g["B"], g.get("C"), D, stream)
+    elif prob["kind"] in ("fp8e4m3", "fp8e5m2"):
+        fmt = tg.GEMM_FP8_E4M3 if prob["kind"] == "fp8e4m3" else tg.GEMM_FP8_E5M2
+        D = torch.empty(M, N, dtype=torch.bfloat16, device=dev) if D is None else D
+        tg.gemm_fp8(g["A"], g["B"], g.get("C"), D, fmt, stream)
     else:
         fmt = tg.GEMM_FMT_NVFP4 if prob["kind"] == "nvfp4" else tg.GEMM_FMT_MXFP8
         D = torch.empty(M, N, dtype=torch.bfloat16, device=dev) if D is None else D
@@ -46,6 +53,10 @@ def oracle_result(prob: dict, rows=None):
     """(rounded output bits uint16 [rows, N], exact fp64 sums [rows, N])."""
     if prob["kind"] == "f16":
         return oracle.gemm_f16(prob["A"], prob["B"], prob.get("C"), rows=rows, exact=True)
+    dense = {"bf16": oracle.BF16, "fp8e4m3": oracle.E4M3, "fp8e5m2": oracle.E5M2}
+    if prob["kind"] in dense:
+        f = dense[prob["kind"]]
+        return oracle.gemm_dense(prob["A"], prob["B"], prob.get("C"), f, f, oracle.BF16, rows=rows, exact=True)
     fmt = oracle.NVFP4 if prob["kind"] == "nvfp4" else oracle.MXFP8
     return oracle.gemm_block_scaled(fmt, prob["A"], prob["SFA"], prob["B"], prob["SFB"],
                                     prob.get("C"), rows=rows, exact=True)
@@ -61,8 +72,12 @@ def _values(t: torch.Tensor) -> np.ndarray:
 
 def operand_max(prob: dict):
     """max |a_real| and max |b_real| (bounds for the block-scaled kinds)."""
-    if prob["kind"] == "f16":
+    if prob["kind"] in ("f16", "bf16"):
         return float(prob["A"].abs().max()), float(prob["B"].abs().max())
+    if prob["kind"] in ("fp8e4m3", "fp8e5m2"):
+        dec = oracle.e4m3_to_f64 if prob["kind"] == "fp8e4m3" else oracle.e5m2_to_f64
+        mx = lambda x: max(abs(dec(int(c))) for c in torch.unique(x))
+        return mx(prob["A"]), mx(prob["B"])
     if prob["kind"] == "nvfp4":
         dec = lambda sf: max(oracle.e4m3_to_f64(int(c)) for c in torch.unique(sf))
         return E2M1_MAX * dec(prob["SFA"]), E2M1_MAX * dec(prob["SFB"])

@@ -78,6 +78,19 @@ def test_f16_noalloc_rejections():
     assert f(64, 64, 64, D=2 * P) == tg.GEMM_ERR_INVALID_ARG
 
 
+def test_bf16_and_fp8_rejections():
+    bf = lambda M, N, K, A=P, B=2 * P, C=None, D=4 * P: tg.lib().gemm_bf16(M, N, K, A, B, C, D, None)
+    f8 = lambda M, N, K, fmt=0, A=P, B=2 * P, C=None, D=4 * P: tg.lib().gemm_fp8(M, N, K, A, B, C, D, fmt, None)
+    assert bf(0, 8, 8) == tg.GEMM_ERR_INVALID_ARG
+    assert bf(8, 8, 12) == tg.GEMM_ERR_ALIGNMENT          # K % 8
+    assert bf(8, 12, 8) == tg.GEMM_ERR_ALIGNMENT          # N % 8
+    assert bf(64, 64, 64, D=2 * P) == tg.GEMM_ERR_INVALID_ARG
+    assert f8(8, 8, 16, fmt=2) == tg.GEMM_ERR_INVALID_ARG
+    assert f8(8, 8, 8) == tg.GEMM_ERR_ALIGNMENT           # K % 16 (16-byte rows)
+    assert f8(8, 8, 16, A=None) == tg.GEMM_ERR_INVALID_ARG
+    assert f8(64, 64, 64, C=4 * P + 16) == tg.GEMM_ERR_INVALID_ARG
+
+
 def test_block_scaled_rejections():
     for fmt in (tg.GEMM_FMT_NVFP4, tg.GEMM_FMT_MXFP8):
         assert _bs(0, 8, 512, fmt) == tg.GEMM_ERR_INVALID_ARG

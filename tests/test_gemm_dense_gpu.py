@@ -1,0 +1,86 @@
+"""GPU parity of the BF16 and unscaled FP8 TN GEMMs against the CPU oracle, through the C ABI."""
+import pytest
+import torch
+
+import cute_layouts_mma_gb300 as tg
+from cute_layouts_mma_gb300 import inputs
+
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+FP8 = ["fp8e4m3", "fp8e5m2"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tg.lib()
+
+
+# ------------------------------------------------------------------ BF16
+
+@pytest.mark.parametrize("M,N,K,with_c", [(384, 520, 512, True), (100, 264, 512, False), (256, 256, 256, True)])
+def test_bf16_integers_bit_exact(M, N, K, with_c):
+    prob = inputs.make_problem("bf16", M, N, K, seed=M + N + K, dist="int2", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (130, 264, 72), (300, 520, 200), (257, 8, 1000),
+                                   (64, 1000, 4096), (1000, 16, 520)])
+def test_bf16_ragged_shapes_tolerance(M, N, K):
+    prob = inputs.make_problem("bf16", M, N, K, seed=M + 2 * N + K, dist="normal0.1", with_c=True)
+    P.check(prob, P.run_gpu(prob), mode="tol")
+
+
+def test_bf16_in_place():
+    prob = inputs.make_problem("bf16", 200, 264, 136, seed=31, dist="int2", with_c=True)
+    g = P.to_device(prob, P.device())
+    D = g["C"].clone()
+    tg.gemm_bf16(g["A"], g["B"], D, D)
+    torch.cuda.synchronize()
+    P.check(prob, D.cpu(), mode="exact")
+
+
+def test_bf16_stream_k_integers_bit_exact():
+    # 10 tiles of 128 x 256 for a 152-SM device, 256 k-blocks: split between units
+    prob = inputs.make_problem("bf16", 128, 2560, 16384, seed=32, dist="int2", with_c=True)
+    P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 16, seed=1), mode="exact")
+
+
+def test_bf16_4096_full_size_sampled_rows():
+    prob = inputs.workload_problem("bf16_4096")
+    D = P.run_gpu(prob)
+    P.check(prob, D, rows=P.sample_rows(prob["M"], 16, seed=2), mode="tol")
+    assert torch.isfinite(D.float()).all()
+
+
+# ------------------------------------------------------------------ FP8 (no scales)
+
+@pytest.mark.parametrize("kind", FP8)
+@pytest.mark.parametrize("M,N,K,with_c", [(256, 264, 1024, True), (100, 512, 512, False), (512, 256, 2048, True)])
+def test_fp8_integers_bit_exact(kind, M, N, K, with_c):
+    prob = inputs.make_problem(kind, M, N, K, seed=M + N, dist="int", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), mode="exact")
+
+
+@pytest.mark.parametrize("kind", FP8)
+@pytest.mark.parametrize("M,N,K", [(1, 8, 16), (130, 264, 96), (257, 8, 1008), (64, 1000, 4096), (300, 392, 1024)])
+def test_fp8_ragged_shapes_tolerance(kind, M, N, K):
+    prob = inputs.make_problem(kind, M, N, K, seed=M + 3 * N + K, dist="normal", with_c=True)
+    P.check(prob, P.run_gpu(prob), mode="tol")
+
+
+@pytest.mark.parametrize("kind", FP8)
+def test_fp8_stream_k_integers_bit_exact(kind):
+    # 8 tiles of 128 x 256, 256 k-blocks of 128: split between units
+    prob = inputs.make_problem(kind, 128, 2048, 32768, seed=33, dist="int", with_c=True)
+    P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 12, seed=3), mode="exact")
+
+
+def test_fp8e4m3_8192_full_size_sampled_rows():
+    prob = inputs.workload_problem("fp8e4m3_8192")
+    D = P.run_gpu(prob)
+    P.check(prob, D, rows=P.sample_rows(prob["M"], 12, seed=4), mode="tol")
+    assert torch.isfinite(D.float()).all()
