@@ -240,27 +240,60 @@ def roofline(w, ms_per_launch, peaks, peak_src):
             "algorithmic_bytes": workload_bytes(w), "algorithmic_flops": w.flops}
 
 
-def e2e_measure(runner, steps: int, stream):
-    """Same metric through the public call with host buffers: per step, pinned host ->
-    device copies of the step's inputs, the GEMM, and a device -> host read of D."""
+def e2e_measure(runner, steps: int, stream, h2d_streams: int = 1):
+    """Same metric through the public call with host buffers.  Every step copies its
+    inputs from pinned host memory to the device, runs the GEMM and reads D back to
+    pinned host memory.  Steps are pipelined over the runner's device buffer sets:
+    the host -> device copies of step i+1 (spread over `h2d_streams` streams, one
+    operand per stream), the GEMM of step i and the device -> host read of step i-1
+    run on separate streams, ordered by events; a set is refilled only after the
+    read of the step that last used it."""
     import torch
-    w, s = runner.w, runner.sets[0]
-    names = [k for k in ("A", "B", "SFA", "SFB", "C") if s.get(k) is not None]
+    sets = runner.sets
+    nsets = len(sets)
+    names = [k for k in ("A", "B", "SFA", "SFB", "C") if sets[0].get(k) is not None]
     host_in = {k: runner.host[k].pin_memory() for k in names}
-    host_out = torch.empty(s["D"].shape, dtype=s["D"].dtype).pin_memory()
+    host_out = [torch.empty(sets[0]["D"].shape, dtype=sets[0]["D"].dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    dev = sets[0]["D"].device
+    in_streams = [torch.cuda.Stream(dev) for _ in range(h2d_streams)]
+    out_stream = torch.cuda.Stream(dev)
+    done_reading = [None] * nsets  # event: last D read of the set finished
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for it in range(steps + 1):
-            if it == 1:
-                start.record(stream)
-            for k in names:
+    torch.cuda.synchronize(dev)
+    total = steps + 2  # two untimed steps fill the pipeline
+    for it in range(total):
+        j = it % nsets
+        s = sets[j]
+        if it == 2:
+            start.record(in_streams[0])
+            for st in in_streams[1:] + [stream, out_stream]:
+                st.wait_stream(in_streams[0])
+        copied = []
+        for n, k in enumerate(names):
+            st = in_streams[n % h2d_streams]
+            if done_reading[j] is not None:
+                st.wait_event(done_reading[j])
+            with torch.cuda.stream(st):
                 s[k].copy_(host_in[k], non_blocking=True)
-            runner.launch(0, stream)
-            host_out.copy_(s["D"], non_blocking=True)
-        end.record(stream)
+            ev = torch.cuda.Event()
+            ev.record(st)
+            copied.append(ev)
+        for ev in copied:
+            stream.wait_event(ev)
+        runner.launch(j, stream)
+        gemm_done = torch.cuda.Event()
+        gemm_done.record(stream)
+        out_stream.wait_event(gemm_done)
+        with torch.cuda.stream(out_stream):
+            host_out[it % 2].copy_(s["D"], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(out_stream)
+        done_reading[j] = done
+    end.record(out_stream)
     end.synchronize()
+    torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / steps
     return ms, h2d, d2h
 
@@ -376,7 +409,10 @@ def gpu_arm(args):
         "roofline": roofline(w, ms, peaks, peak_src),
         "clocks": clocks.summary(),
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "method": "per step: pinned host -> device copy of A, B (and C / scales), the GEMM, device -> "
+                          "pinned host read of D; steps pipelined over the device buffer sets (copies of "
+                          "step i+1, GEMM of step i and read of step i-1 overlap on three streams)"},
         "gpu_launches": args.steps,
         "timing": "CUDA-graph replay of the K launches" if not args.no_graph else "back-to-back launches",
     }

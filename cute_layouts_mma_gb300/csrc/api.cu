@@ -85,6 +85,7 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
     const cuuint32_t elem_strides[2] = {1, 1};
     const CUtensorMapSwizzle swz = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                   : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                                          : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

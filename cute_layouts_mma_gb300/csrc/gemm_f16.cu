@@ -12,6 +12,15 @@ using CfgF16Acc16Pair = Config<KIND_F16_ACC16, 256, 6, 2, 64, 2, 2>;
 // Single CTAs (M <= 128): 128 x 256 tiles, 4 stages.
 using CfgF16Acc32 = Config<KIND_F16_ACC32, 256, 4, 2, 64, 2, 1>;
 using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
+// Narrow K (fp32 accumulation): a whole K of at most 32 or 16 elements fits a 64- or
+// 32-byte operand row, stored with the 64- or 32-byte swizzle; 2 or 1 MMAs per stage
+// instead of 4 over zero-filled K.  These launches are bound by the C and D traffic,
+// so the small stages leave room to stage a warp's whole 32 x 256 slice (C for the
+// tile is fetched before its accumulator is ready).
+using CfgF16K32Pair = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 2, 4, 64>;
+using CfgF16K32 = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 1, 4, 64>;
+using CfgF16K16Pair = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 2, 4, 32>;
+using CfgF16K16 = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 1, 4, 32>;
 
 // Device-side record of an abandoned launch (a bounded wait ran out).
 static __device__ unsigned int g_err_f16;
@@ -35,10 +44,12 @@ template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
                   cudaStream_t stream, int sms, int dev) {
     CUtensorMap ta, tb, td, tc;
-    // A: fp16 [M][K], 128-row boxes; B: fp16 [N][K], BN/PAIR-row boxes; 64 elements
-    // (128 bytes) of K per box.  D: fp16 [M][N], stored in 32-row x EPI_COLS boxes.
-    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, 64, Cfg::BM, 128) ||
-        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, 64, Cfg::BN_CTA, 128) ||
+    // A: fp16 [M][K], 128-row boxes; B: fp16 [N][K], BN/PAIR-row boxes; kRowBytes
+    // (128, or 64 / 32 for narrow K) of K per box, swizzled to match.  D: fp16 [M][N],
+    // stored in 32-row x EPI_COLS boxes.
+    constexpr int kKBox = Cfg::kKCoordPerStage, kSw = Cfg::kRowBytes;
+    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, kKBox, Cfg::BM, kSw) ||
+        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, kKBox, Cfg::BN_CTA, kSw) ||
         !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
                        Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;
@@ -55,7 +66,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
     p.K = static_cast<int>(K);
     p.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
     p.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
-    p.num_k_blocks = static_cast<int>((K + 63) / 64);
+    p.num_k_blocks = static_cast<int>((K + kKBox - 1) / kKBox);
     p.C = C;
     p.D = D;
     p.err = err;
@@ -68,9 +79,16 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
 gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                               void* D, int accum, cudaStream_t stream, int sms, int dev) {
     const bool pair = M > 128;
-    if (accum == GEMM_ACC_F32)
+    if (accum == GEMM_ACC_F32) {
+        if (K <= 16)
+            return pair ? run<CfgF16K16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                        : run<CfgF16K16>(M, N, K, A, B, C, D, stream, sms, dev);
+        if (K <= 32)
+            return pair ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                        : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
         return pair ? run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                     : run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+    }
     return pair ? run<CfgF16Acc16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                 : run<CfgF16Acc16>(M, N, K, A, B, C, D, stream, sms, dev);
 }

@@ -135,7 +135,7 @@ __device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it
 }
 
 template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
-          int EPI_WARPS_ = 4>
+          int EPI_WARPS_ = 4, int ROW_BYTES_ = 128>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
@@ -170,12 +170,18 @@ struct Config {
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
     // writers, 12 SFB issuer, 13-16 second epilogue set
     static constexpr int THREADS = EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256);
-    static constexpr int kMmasPerStage = 4;  // 128 bytes of K per stage, 32 bytes per MMA
+    // Bytes of K per operand row and stage: 128 (the 128-byte swizzle), or 64 / 32 for
+    // problems whose whole K is narrower ("数据布局及其记号", swizzle section: the same
+    // hierarchy with 8 x 64-byte and 8 x 32-byte atoms).  32 bytes of K per MMA.
+    static constexpr int kRowBytes = ROW_BYTES_;
+    static_assert(kRowBytes == 128 || kRowBytes == 64 || kRowBytes == 32, "128-, 64- or 32-byte operand rows");
+    static_assert(kRowBytes == 128 || is_dense(KIND_), "block-scaled stages hold 128 bytes of K");
+    static constexpr int kMmasPerStage = kRowBytes / 32;
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
-    static constexpr int kKCoordPerStage = operands_16bit(KIND) ? 64 : 128;
+    static constexpr int kKCoordPerStage = operands_16bit(KIND) ? kRowBytes / 2 : kRowBytes;
 
-    static constexpr int A_BYTES = BM * 128;
-    static constexpr int B_BYTES = BN_CTA * 128;
+    static constexpr int A_BYTES = BM * kRowBytes;
+    static constexpr int B_BYTES = BN_CTA * kRowBytes;
     static constexpr int SFB_GROUPS = kBlockScaled ? (BN + 127) / 128 : 0;  // 128-row scale groups
     static constexpr int SFA_BYTES = kBlockScaled ? BM * 16 : 0;
     static constexpr int SFB_BYTES = SFB_GROUPS * 128 * 16;
@@ -603,8 +609,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // and the shared-memory descriptors precomputed.
             constexpr uint32_t kM = 128 * PAIR;
             // descriptor of stage 0; stage s adds s * (bytes / 16) to the start address
-            const uint64_t adesc0 = smem_desc_sw128(sbase + Cfg::OFF_A);
-            const uint64_t bdesc0 = smem_desc_sw128(sbase + Cfg::OFF_B);
+            const uint64_t adesc0 = layout::umma_smem_desc_kmajor(sbase + Cfg::OFF_A, Cfg::kRowBytes);
+            const uint64_t bdesc0 = layout::umma_smem_desc_kmajor(sbase + Cfg::OFF_B, Cfg::kRowBytes);
             bool ok = true;
             int s = 0;
             uint32_t ph = 0;
@@ -635,12 +641,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint64_t adesc = adesc0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
                     const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s * (Cfg::B_BYTES >> 4));
                     if constexpr (is_dense(KIND)) {
-                        // 4 MMAs of 32 bytes of K: 16 elements (kind::f16) or 32 (kind::f8f6f4)
+                        // MMAs of 32 bytes of K: 16 elements (kind::f16) or 32 (kind::f8f6f4)
                         constexpr uint32_t idesc =
                             idesc_dense(kM, BN, KIND != KIND_F16_ACC16,
                                         (KIND == KIND_BF16 || KIND == KIND_FP8_E5M2) ? 1u : 0u);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
+                        for (int j = 0; j < Cfg::kMmasPerStage; ++j) {
                             if constexpr (operands_16bit(KIND)) {
                                 if constexpr (kPair)
                                     mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);

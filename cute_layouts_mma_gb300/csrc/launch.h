@@ -12,7 +12,7 @@ namespace tn {
 
 // Encode a 2-D tiled TMA map over a row-major matrix: `inner` elements per row
 // (contiguous), `rows` rows `pitch` bytes apart, boxes of box_inner x box_rows.
-// swizzle_bytes: 0 (none), 64 or 128 -- the XOR swizzle of the box in shared
+// swizzle_bytes: 0 (none), 32, 64 or 128 -- the XOR swizzle of the box in shared
 // memory (box rows of at most that many bytes).  Maps are cached per thread.
 // Returns false if the driver rejects the map.
 bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,

@@ -244,16 +244,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // ------------------------------------------------------------------ descriptors
 
-// Shared-memory matrix descriptor, K-major operand tile of 128-byte rows written
-// by TMA with the 128-byte swizzle: 8-row x 128-byte atoms (1024 bytes) stacked
-// along M/N, so the stride between 8-row groups is 1024 bytes.  The 16-byte
-// sector s of row r sits at sector s ^ (r % 8) ("数据布局及其记号", section
-// "Swizzle Layout").  Stepping K inside the 128-byte row adds bytes to the start
-// address; the tile base is 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    return layout::umma_smem_desc_kmajor(saddr, 128);
-}
-
 // Instruction descriptor of the dense kinds, both operands K-major, M x N tile,
 // D in fp32 (d_f32) or fp16.  ab_format is the operand type code of the kind:
 // kind::f16 0 = F16, 1 = BF16; kind::f8f6f4 0 = E4M3, 1 = E5M2 (A and B alike).

@@ -99,6 +99,20 @@ def test_fp16_pairs_long_k_whole_tiles(M, N, K, rows):
     P.check(prob, D, rows=None if rows is None else P.sample_rows(M, rows, seed=7), mode="tol")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 264, 32), (128, 520, 16), (300, 256, 8), (100, 136, 24),
+                                   (1000, 1000, 32), (129, 8, 16)])
+def test_fp16_narrow_k_integers_bit_exact(M, N, K):
+    # K of at most 32 / 16 elements: 64- / 32-byte operand rows with the matching swizzle
+    prob = inputs.make_problem("f16", M, N, K, seed=M + K, dist="int2", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), mode="exact")
+
+
+@pytest.mark.parametrize("M,N,K", [(513, 384, 32), (64, 256, 16), (2048, 2048, 24)])
+def test_fp16_narrow_k_random_tolerance(M, N, K):
+    prob = inputs.make_problem("f16", M, N, K, seed=M + N + K, dist="normal0.1", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), mode="tol")
+
+
 def test_fp16acc_integers_bit_exact():
     # every partial sum is an integer of magnitude <= 1024: exact in fp16
     prob = inputs.make_problem("f16", 256, 264, 256, seed=11, dist="int2", with_c=False)
