@@ -40,10 +40,10 @@ unsigned int* err_word(int dev) {
     return reinterpret_cast<unsigned int*>(a);
 }
 
+// Tensor maps and kernel parameters of one FP16 launch.
 template <class Cfg>
-gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
-                  cudaStream_t stream, int sms, int dev) {
-    CUtensorMap ta, tb, td, tc;
+gemm_status_t prepare(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                      int dev, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& td, CUtensorMap& tc, Params& p) {
     // A: fp16 [M][K], 128-row boxes; B: fp16 [N][K], BN/PAIR-row boxes; kRowBytes
     // (128, or 64 / 32 for narrow K) of K per box, swizzled to match.  D: fp16 [M][N],
     // stored in 32-row x EPI_COLS boxes.
@@ -60,7 +60,6 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
         return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (err == nullptr) return GEMM_ERR_CUDA;
-    Params p;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -70,6 +69,16 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
     p.C = C;
     p.D = D;
     p.err = err;
+    return GEMM_OK;
+}
+
+template <class Cfg>
+gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                  cudaStream_t stream, int sms, int dev) {
+    CUtensorMap ta, tb, td, tc;
+    Params p;
+    const gemm_status_t st = prepare<Cfg>(M, N, K, A, B, C, D, dev, ta, tb, td, tc, p);
+    if (st != GEMM_OK) return st;
     if (launch_config<Cfg>(ta, tb, ta, tb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -123,30 +132,12 @@ template <class Cfg>
 gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
                           cudaStream_t stream, int sms, int dev) {
     CUtensorMap ta, tb, td, tc;
-    if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, 64, Cfg::BM, 128) ||
-        !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, 64, Cfg::BN_CTA, 128) ||
-        !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
-                       Cfg::EPI_ROW_BYTES))
-        return GEMM_ERR_CUDA;
-    if (C == nullptr)
-        tc = td;
-    else if (!encode_tma_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, N, M, N * 2, Cfg::EPI_COLS, 32, Cfg::EPI_ROW_BYTES))
-        return GEMM_ERR_CUDA;
-    unsigned int* err = err_word(dev);
-    void* scratch = static_scratch(dev);
-    if (err == nullptr || scratch == nullptr) return GEMM_ERR_CUDA;
     Params p;
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
-    p.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
-    p.num_k_blocks = static_cast<int>((K + 63) / 64);
-    p.C = C;
-    p.D = D;
-    p.err = err;
-    const gemm_status_t st =
-        launch_config_fixed_scratch<Cfg>(ta, tb, td, tc, p, sms, dev, stream, scratch, kStaticScratchBytes);
+    gemm_status_t st = prepare<Cfg>(M, N, K, A, B, C, D, dev, ta, tb, td, tc, p);
+    if (st != GEMM_OK) return st;
+    void* scratch = static_scratch(dev);
+    if (scratch == nullptr) return GEMM_ERR_CUDA;
+    st = launch_config_fixed_scratch<Cfg>(ta, tb, td, tc, p, sms, dev, stream, scratch, kStaticScratchBytes);
     if (st != GEMM_OK) return st;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

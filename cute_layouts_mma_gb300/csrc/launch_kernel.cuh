@@ -62,17 +62,20 @@ Schedule choose_schedule(const Params& p, int max_units) {
     return Schedule{max_units, static_cast<int>(split)};
 }
 
+// Launch configuration shared by every launch of Cfg: block, shared memory, stream,
+// the (2,1,1) cluster of CTA pairs.  On first use per device it sets the kernel's
+// shared-memory attribute and finds the units (resident CTAs, or clusters for
+// PAIR = 2) the device keeps at once.
 template <class Cfg>
-cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                          const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& tc, Params p,
-                          int sms, int dev, cudaStream_t stream) {
+cudaError_t prepare_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int sms, int dev,
+                           cudaStream_t stream, int* units_out) {
     auto kernel = tn_gemm_kernel<Cfg>;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cfg = cudaLaunchConfig_t{};
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
+    cfg.numAttrs = 0;
     if (Cfg::PAIR == 2) {
         attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
         attr[cfg.numAttrs].val.clusterDim.x = 2;
@@ -84,21 +87,27 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     if (units == 0) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        units = sms;
         if (Cfg::PAIR == 2) {
             cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
             int clusters = 0;
             e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
             if (e != cudaSuccess) return e;
             units = clusters > 0 ? clusters : sms / 2;
-        } else {
-            units = sms;
         }
         LaunchState<Cfg>::max_units[dev].store(units, std::memory_order_release);
     }
+    *units_out = units;
+    return cudaSuccess;
+}
+
+// Grid, stream-K fields of `p` and the programmatic-dependent-launch attribute for
+// one launch: the kernel's set-up may overlap the previous launch on the stream;
+// it waits (griddepcontrol.wait) before touching global memory.
+template <class Cfg>
+Schedule apply_schedule(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], Params& p, int units) {
     const Schedule sc = choose_schedule<Cfg>(p, units);
     cfg.gridDim = dim3(sc.units * Cfg::PAIR, 1, 1);
-    // The kernel's set-up may overlap the previous launch on the stream; it waits
-    // (griddepcontrol.wait) before touching global memory.
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
     ++cfg.numAttrs;
@@ -106,17 +115,30 @@ cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     p.sk_total = static_cast<long long>(sc.sk_tiles) * p.num_k_blocks;
     p.ws = nullptr;
     p.flags = nullptr;
-    if (sc.sk_tiles == 0) return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, tc, p);
+    return sc;
+}
+
+template <class Cfg>
+cudaError_t launch_config(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                          const CUtensorMap& tsb, const CUtensorMap& td, const CUtensorMap& tc, Params p,
+                          int sms, int dev, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    int units = 0;
+    cudaError_t e = prepare_launch<Cfg>(cfg, attr, sms, dev, stream, &units);
+    if (e != cudaSuccess) return e;
+    const Schedule sc = apply_schedule<Cfg>(cfg, attr, p, units);
+    if (sc.sk_tiles == 0) return cudaLaunchKernelEx(&cfg, tn_gemm_kernel<Cfg>, ta, tb, tsa, tsb, td, tc, p);
     // Stream-K scratch: taken from the device's stream-ordered pool for this call
     // and returned on the same stream after the kernel.
     const size_t pbytes = sk_partial_bytes<Cfg>(sc.units), fbytes = sk_flag_bytes<Cfg>(sc.units);
     void* scratch = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&scratch, pbytes + fbytes, scratch_pool(dev), stream);
+    e = cudaMallocFromPoolAsync(&scratch, pbytes + fbytes, scratch_pool(dev), stream);
     if (e != cudaSuccess) return e;
     p.ws = static_cast<float*>(scratch);
     p.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(scratch) + pbytes);
     e = cudaMemsetAsync(p.flags, 0, fbytes, stream);
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, td, tc, p);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, tn_gemm_kernel<Cfg>, ta, tb, tsa, tsb, td, tc, p);
     const cudaError_t f = cudaFreeAsync(scratch, stream);
     return e != cudaSuccess ? e : f;
 }
@@ -131,45 +153,11 @@ template <class Cfg>
 gemm_status_t launch_config_fixed_scratch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                                           const CUtensorMap& tc, Params p, int sms, int dev, cudaStream_t stream,
                                           void* scratch, size_t capacity) {
-    auto kernel = tn_gemm_kernel<Cfg>;
-    cudaLaunchConfig_t cfg = {};
+    cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    if (Cfg::PAIR == 2) {
-        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
-        attr[cfg.numAttrs].val.clusterDim.x = 2;
-        attr[cfg.numAttrs].val.clusterDim.y = 1;
-        attr[cfg.numAttrs].val.clusterDim.z = 1;
-        ++cfg.numAttrs;
-    }
-    int units = LaunchState<Cfg>::max_units[dev].load(std::memory_order_acquire);
-    if (units == 0) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
-            cudaSuccess)
-            return GEMM_ERR_CUDA;
-        units = sms;
-        if (Cfg::PAIR == 2) {
-            cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-            int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) return GEMM_ERR_CUDA;
-            units = clusters > 0 ? clusters : sms / 2;
-        }
-        LaunchState<Cfg>::max_units[dev].store(units, std::memory_order_release);
-    }
-    const Schedule sc = choose_schedule<Cfg>(p, units);
-    cfg.gridDim = dim3(sc.units * Cfg::PAIR, 1, 1);
-    // The kernel's set-up may overlap the previous launch on the stream; it waits
-    // (griddepcontrol.wait) before touching global memory.
-    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
-    ++cfg.numAttrs;
-    p.sk_tiles = sc.sk_tiles;
-    p.sk_total = static_cast<long long>(sc.sk_tiles) * p.num_k_blocks;
-    p.ws = nullptr;
-    p.flags = nullptr;
+    int units = 0;
+    if (prepare_launch<Cfg>(cfg, attr, sms, dev, stream, &units) != cudaSuccess) return GEMM_ERR_CUDA;
+    const Schedule sc = apply_schedule<Cfg>(cfg, attr, p, units);
     if (sc.sk_tiles != 0) {
         const size_t pbytes = sk_partial_bytes<Cfg>(sc.units), fbytes = sk_flag_bytes<Cfg>(sc.units);
         if (scratch == nullptr || pbytes + fbytes > capacity) return GEMM_ERR_INVALID_ARG;
@@ -177,7 +165,8 @@ gemm_status_t launch_config_fixed_scratch(const CUtensorMap& ta, const CUtensorM
         p.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(scratch) + pbytes);
         if (cudaMemsetAsync(p.flags, 0, fbytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     }
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, ta, tb, td, tc, p) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, tn_gemm_kernel<Cfg>, ta, tb, ta, tb, td, tc, p) == cudaSuccess ? GEMM_OK
+                                                                                               : GEMM_ERR_CUDA;
 }
 
 }  // namespace tn
