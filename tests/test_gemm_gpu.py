@@ -263,6 +263,34 @@ def test_stream_k_mxfp8_random_tolerance():
     P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 12, seed=5), mode="tol")
 
 
+# ------------------------------------------------------------------ large extents
+# One very long dimension at a time (the ABI takes each of M, N, K below 2^31; these
+# stay within a few hundred MB of device memory).  Integer inputs keep every fp32
+# partial sum exact, so sampled rows must match bit for bit.
+
+def test_large_k_fp16_single_tile_split_over_all_units():
+    # K = 2^20: one 128 x 256 tile whose 16384 k-blocks are split across every unit
+    prob = inputs.make_problem("f16", 128, 128, 1 << 20, seed=51, dist="int2", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), rows=[0, 1, 63, 127], mode="exact")
+
+
+def test_large_m_fp16_narrow_k():
+    prob = inputs.make_problem("f16", 1 << 20, 16, 16, seed=52, dist="int2", with_c=True)
+    D = P.run_gpu(prob, accum=0)
+    P.check(prob, D, rows=P.sample_rows(1 << 20, 24, seed=5), mode="exact")
+
+
+def test_large_n_fp16():
+    prob = inputs.make_problem("f16", 128, 1 << 20, 32, seed=53, dist="int2", with_c=False)
+    D = P.run_gpu(prob, accum=0)
+    P.check(prob, D, rows=[0, 77, 127], mode="exact")
+
+
+def test_large_k_nvfp4():
+    prob = inputs.make_problem("nvfp4", 128, 256, 1 << 18, seed=54, dist="int", with_c=True)
+    P.check(prob, P.run_gpu(prob), rows=[0, 31, 127], mode="exact")
+
+
 # ------------------------------------------------------------------ argument errors on the GPU
 
 def test_misaligned_output_is_rejected_not_faulted():
