@@ -298,17 +298,50 @@ def e2e_measure(runner, steps: int, stream, h2d_streams: int = 1):
     return ms, h2d, d2h
 
 
-def oracle_rows(w, p, rows):
-    """The oracle's result for the given rows of workload w's problem p."""
+def oracle_rows(w, p, rows, exact: bool = False):
+    """The oracle's result for the given rows of workload w's problem p (output bits,
+    plus the unrounded fp64 sums when exact)."""
     import oracle
     if w.kind == "f16":
-        return oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows)
+        return oracle.gemm_f16(p["A"], p["B"], p.get("C"), rows=rows, exact=exact)
     dense = {"bf16": oracle.BF16, "fp8e4m3": oracle.E4M3, "fp8e5m2": oracle.E5M2}
     if w.kind in dense:
         f = dense[w.kind]
-        return oracle.gemm_dense(p["A"], p["B"], p.get("C"), f, f, oracle.BF16, rows=rows)
+        return oracle.gemm_dense(p["A"], p["B"], p.get("C"), f, f, oracle.BF16, rows=rows, exact=exact)
     fmt = oracle.NVFP4 if w.kind == "nvfp4" else oracle.MXFP8
-    return oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows)
+    return oracle.gemm_block_scaled(fmt, p["A"], p["SFA"], p["B"], p["SFB"], p.get("C"), rows=rows, exact=exact)
+
+
+def operand_bounds(w, p):
+    """max |a| and max |b| of the decoded (scaled) operands."""
+    import torch
+    if w.kind in ("f16", "bf16"):
+        return float(p["A"].float().abs().max()), float(p["B"].float().abs().max())
+    if w.kind in ("fp8e4m3", "fp8e5m2", "mxfp8"):
+        dt = torch.float8_e5m2 if w.kind == "fp8e5m2" else torch.float8_e4m3fn
+        mx = lambda x: float(x.view(dt).float().abs().max())
+        if w.kind != "mxfp8":
+            return mx(p["A"]), mx(p["B"])
+        sf = lambda x: float(2.0 ** (x.max().item() - 127))
+        return mx(p["A"]) * sf(p["SFA"]), mx(p["B"]) * sf(p["SFB"])
+    sf = lambda x: float(x.view(torch.float8_e4m3fn).float().max())
+    return 6.0 * sf(p["SFA"]), 6.0 * sf(p["SFB"])  # E2M1 magnitudes reach 6
+
+
+def parity_of(w, p, rows, d64, D):
+    """GPU output rows against the oracle's exact sums: |D - exact| <= 1e-3*sqrt(K)*max|a|*max|b|
+    plus half an output ulp (the tolerance the parity tests use)."""
+    import numpy as np
+    import torch
+    got = D[rows].float().cpu().double().numpy()
+    err = np.abs(got - d64)
+    a, b = operand_bounds(w, p)
+    tol = 1e-3 * math.sqrt(w.K) * a * b
+    mbits, emin = (10, -14) if w.kind == "f16" else (7, -126)
+    half_ulp = 0.5 * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(d64), 2.0 ** emin))) - mbits)
+    return {"rows": len(rows), "max_abs_err": float(err.max()), "tolerance": tol,
+            "ok": bool((err <= tol + half_ulp).all() and np.isfinite(got).all()),
+            "rule": "|D - exact| <= 1e-3*sqrt(K)*max|a|*max|b| + half an output ulp, on the cpu_baseline rows"}
 
 
 def cpu_baseline(w, budget_s: float):
@@ -318,9 +351,11 @@ def cpu_baseline(w, budget_s: float):
     from cute_layouts_mma_gb300 import inputs
     p = inputs.make_problem(w.kind, w.M, w.N, w.K, w.seed, w.dist, w.with_c)
 
+    out = {}
+
     def run(rows):
         t0 = time.perf_counter()
-        oracle_rows(w, p, rows)
+        out["d16"], out["d64"] = oracle_rows(w, p, rows, exact=True)
         return time.perf_counter() - t0
 
     threads = oracle.num_threads()
@@ -333,7 +368,8 @@ def cpu_baseline(w, budget_s: float):
     t = run(rows)
     tflops = 2.0 * nrows * w.N * w.K / t / 1e12
     return {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{nrows} of {w.M} output rows (all N columns), fp64 oracle, {t:.1f} s"}, t
+            "sample": f"{nrows} of {w.M} output rows (all N columns), fp64 oracle, {t:.1f} s"}, t, \
+        (p, rows, out["d64"])
 
 
 def reduce_max(value: float, world: int, device) -> float:
@@ -434,8 +470,10 @@ def gpu_arm(args):
         assert runner.tg.gemm_last_device_error() == runner.tg.GEMM_OK
         line["per_workload"] = extras
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb, _ = cpu_baseline(w, args.cpu_seconds)
+        cb, _, (p, rows, d64) = cpu_baseline(w, args.cpu_seconds)
         line["cpu_baseline"] = cb
+        # the timed launches' own output (set 0), checked on the oracle's rows
+        line["parity"] = parity_of(w, p, rows, d64, runner.sets[0]["D"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
