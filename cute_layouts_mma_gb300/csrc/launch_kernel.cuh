@@ -66,6 +66,19 @@ Schedule choose_schedule(const Params& p, int max_units) {
 // the (2,1,1) cluster of CTA pairs.  On first use per device it sets the kernel's
 // shared-memory attribute and finds the units (resident CTAs, or clusters for
 // PAIR = 2) the device keeps at once.
+// Whether Cfg's own schedule would split tiles for this problem (units estimated
+// as one per SM, or one per SM pair).  The launchers then switch to their
+// 128-column instance: half as many pieces per split tile and half the partial
+// bytes per piece, which measured 1.2-1.8x faster on such skinny problems.
+template <class Cfg>
+bool would_split(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
+    Params q{};
+    q.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
+    q.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
+    q.num_k_blocks = static_cast<int>((K + k_per_block - 1) / k_per_block);
+    return choose_schedule<Cfg>(q, Cfg::PAIR == 2 ? sms / 2 : sms).sk_tiles != 0;
+}
+
 template <class Cfg>
 cudaError_t prepare_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int sms, int dev,
                            cudaStream_t stream, int* units_out) {
