@@ -58,10 +58,16 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: whole-line comments and blank lines are left
+    out, so that recorded counters stay attached to unchanged code."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                t = line.strip()
+                if t and not t.startswith("//"):
+                    h.update(t.encode())
+                    h.update(b"\n")
     return h.hexdigest()[:16]
 
 

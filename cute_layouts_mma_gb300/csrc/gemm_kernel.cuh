@@ -1,7 +1,13 @@
 // Persistent, warp-specialised TN GEMM for sm_103a:  D = A x B^T + C  with A (M,K)
 // and B (N,K) K-contiguous ("CuTe 中 A、B 如何加载到 MMA 寄存器", section 1), in
-// FP16 or in the block-scaled NVFP4 / MXFP8 forms ("数据布局及其记号", block-scaled
-// MMA section).
+// FP16, BF16 or FP8, or in the block-scaled NVFP4 / MXFP8 forms ("数据布局及其记号",
+// block-scaled MMA section).
+//
+// Work is dealt to persistent units (CTAs, or CTA pairs) either as whole tiles,
+// round robin, or -- for skinny problems that would leave most units idle -- as a
+// stream-K split of the tiles' k-blocks (see Params).  The set-up overlaps the
+// previous launch on the stream (programmatic dependent launch); global memory is
+// touched only after griddepcontrol.wait.
 //
 // Output tiles are (128 * PAIR) x BN.  With PAIR = 2 the two CTAs of a (2,1,1)
 // cluster share a tile: CTA r loads A rows 128r .. 128r+127 and B rows
@@ -11,8 +17,9 @@
 // halves the B bytes loaded from L2 and read by the tensor core.
 //
 // Warps of each CTA:
-//   warps 0, 2   TMA issuers for A and B: per 128-byte K slice, load this CTA's A
-//                (warp 0) and B (warp 2) box into 128B-swizzled shared memory and
+//   warps 0, 2   TMA issuers for A and B: per K slice of kRowBytes (128, or 64 / 32
+//                for narrow K), load this CTA's A (warp 0) and B (warp 2) box into
+//                swizzled shared memory and
 //                arm the leader's `full` barrier with the bytes (PAIR = 2: the
 //                peer's copies signal the leader's barrier directly).  A TMA
 //                instruction occupies its issuing warp for a few hundred cycles
@@ -20,16 +27,18 @@
 //   warps 3, 12  (block-scaled only) TMA issuers of the raw scale boxes (this
 //                CTA's 128 SFA rows, all BN SFB rows of the tile) on `sf_full`.
 //   warp 1       TMEM allocation; in the leader, the MMA issuer (one thread):
-//                tcgen05.mma into a TMEM accumulator, four K steps per stage;
+//                tcgen05.mma into a TMEM accumulator, 32 bytes of K per MMA;
 //                tcgen05.commit frees the stage (`empty`, in both CTAs) and, at the
 //                end of a tile, hands the accumulator to the epilogues
 //                (`tmem_full`, in both CTAs).
-//   warps 4-7    epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//                32*(w%4) .. +31, i.e. rows of the tile), adds C in fp32, rounds
+//   warps 4-7    epilogue (and 13-16 in the 8-epilogue-warp instance): tcgen05.ld
+//                of the accumulator (warp w reads TMEM lanes 32*(w%4) .. +31, i.e.
+//                rows of the tile), adds any stream-K partials and C in fp32, rounds
 //                once to fp16 / bf16, writes the 32-row chunk to a swizzled
 //                shared-memory staging buffer and TMA-stores it (the store clips
 //                rows / columns outside D); then releases the accumulator on the
-//                leader's `tmem_empty`.
+//                leader's `tmem_empty`.  A stream-K piece that does not finish its
+//                tile instead writes its fp32 sums to scratch and raises a flag.
 //   warps 8-11   (block-scaled only) scale writers, one per TMEM lane quarter:
 //                each turns the stage's row-major scale boxes into the 32-lane
 //                base tiles the block-scaled MMA reads (local_lane = m % 32,
