@@ -84,3 +84,50 @@ def test_fp8e4m3_8192_full_size_sampled_rows():
     D = P.run_gpu(prob)
     P.check(prob, D, rows=P.sample_rows(prob["M"], 12, seed=4), mode="tol")
     assert torch.isfinite(D.float()).all()
+
+
+# ------------------------------------------------------------------ in place, guard bands, concurrency
+
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp8", "fp8e4m3"])
+def test_in_place_d_is_c(kind):
+    M, N, K = (300, 264, 1024) if kind != "mxfp8" else (200, 256, 1024)
+    prob = inputs.make_problem(kind, M, N, K, seed=61, dist="int", with_c=True)
+    g = P.to_device(prob, P.device())
+    D = g["C"].clone()
+    if kind == "fp8e4m3":
+        tg.gemm_fp8(g["A"], g["B"], D, D, tg.GEMM_FP8_E4M3)
+    else:
+        fmt = tg.GEMM_FMT_NVFP4 if kind == "nvfp4" else tg.GEMM_FMT_MXFP8
+        tg.gemm_block_scaled(g["A"], g["SFA"], g["B"], g["SFB"], D, D, fmt)
+    torch.cuda.synchronize()
+    P.check(prob, D.cpu(), mode="exact")
+
+
+@pytest.mark.parametrize("kind,M,N,K", [("nvfp4", 130, 264, 512), ("fp8e5m2", 129, 136, 1008), ("bf16", 257, 8, 72)])
+def test_guard_bands_untouched(kind, M, N, K):
+    # D sits between NaN guard bands; ragged M and N must not write outside it
+    prob = inputs.make_problem(kind, M, N, K, seed=62, dist="int" if kind != "bf16" else "int2", with_c=True)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), float("nan"), dtype=torch.bfloat16, device=P.device())
+    D = buf[pad:pad + M * N].view(M, N)
+    P.run_gpu(prob, D=D)
+    host = buf.cpu()
+    assert torch.isnan(host[:pad].float()).all() and torch.isnan(host[pad + M * N:].float()).all()
+    P.check(prob, D.cpu(), mode="exact")
+
+
+def test_concurrent_stream_k_calls_on_two_streams():
+    # two split launches in flight at once take separate scratch from the pool
+    probs = [inputs.make_problem("f16", 128, 2560, 16384, seed=63 + i, dist="int2", with_c=True) for i in range(2)]
+    dev = P.device()
+    gs = [P.to_device(p, dev) for p in probs]
+    Ds = [torch.empty(128, 2560, dtype=torch.float16, device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for g, D, s in zip(gs, Ds, streams):
+            tg.gemm_f16(g["A"], g["B"], g["C"], D, tg.GEMM_ACC_F32, s)
+    torch.cuda.synchronize()
+    assert tg.gemm_last_device_error() == tg.GEMM_OK
+    for p, D in zip(probs, Ds):
+        P.check(p, D.cpu(), rows=P.sample_rows(128, 16, seed=8), mode="exact")
