@@ -15,9 +15,11 @@ using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 2, 2, 8>;
 // 1.2-1.75x faster than 128 x 256 tiles with one accumulator on skinny problems:
 // the next tile's MMAs no longer wait for the drain, and stream-K cuts fewer pieces.
 using CfgNvfp4 = Config<KIND_NVFP4, 128, 6, 2, 32, 1, 1>;
-// MXFP8: 128 x 128 tiles, 6 stages, double-buffered accumulator (one CTA per
-// MMA: the skinny, HBM-bound shape is M = 128).
-using CfgMxfp8 = Config<KIND_MXFP8, 128, 6, 2, 32, 1, 1>;
+// MXFP8: 128 x 128 tiles, 5 stages, double-buffered accumulator (one CTA per
+// MMA: the skinny, HBM-bound shape is M = 128).  Each epilogue warp stages its whole
+// 32 x 128 slice, so all of C for a tile is fetched before the accumulator is ready
+// (a one-tile-per-CTA problem otherwise pays the C round trips after its mainloop).
+using CfgMxfp8 = Config<KIND_MXFP8, 128, 5, 2, 32, 4, 1>;
 
 static __device__ unsigned int g_err_bs;
 
