@@ -10,11 +10,12 @@ namespace tn {
 // (the scale slots use the rest); 8 epilogue warps each stage a whole 32 x 128
 // slice, so the accumulator is released before any store is issued.
 using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 2, 2, 8>;
-// NVFP4, single CTAs (M <= 128): 128 x 128 tiles, 6 stages, two TMEM accumulators
-// (2 x 128 + 6 x 32 scale columns), epilogue staged in 32 x 32 chunks.  Measured
-// 1.2-1.75x faster than 128 x 256 tiles with one accumulator on skinny problems:
-// the next tile's MMAs no longer wait for the drain, and stream-K cuts fewer pieces.
-using CfgNvfp4 = Config<KIND_NVFP4, 128, 6, 2, 32, 1, 1>;
+// NVFP4, single CTAs (M <= 128): 128 x 128 tiles, 5 stages, two TMEM accumulators
+// (2 x 128 + 5 x 32 scale columns), each epilogue warp staging its whole 32 x 128
+// slice.  Measured 1.2-1.75x faster than 128 x 256 tiles with one accumulator on
+// skinny problems: the next tile's MMAs no longer wait for the drain, and stream-K
+// cuts fewer pieces.
+using CfgNvfp4 = Config<KIND_NVFP4, 128, 5, 2, 32, 4, 1>;
 // MXFP8: 128 x 128 tiles, 5 stages, double-buffered accumulator (one CTA per
 // MMA: the skinny, HBM-bound shape is M = 128).  Each epilogue warp stages its whole
 // 32 x 128 slice, so all of C for a tile is fetched before the accumulator is ready
