@@ -239,8 +239,14 @@ def roofline(w, ms_per_launch, peaks, peak_src):
         achieved = workload_bytes(w) / (ms_per_launch * 1e-3) / 1e9
     else:
         achieved = w.flops / (ms_per_launch * 1e-3) / 1e12
+    extra = {}
+    if bound == "tensor":
+        # the timed region follows a second of untimed launches, so the part runs at its
+        # power-capped steady state: also state the fraction of the sustained peak
+        sustained = peaks["bf16_tflops_sustained"] * NOMINAL_RATIO[w.kind]
+        extra = {"peak_sustained": sustained, "frac_sustained": round(achieved / sustained, 4)}
     return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+            "frac": round(achieved / peak, 4), **extra, "traffic": recorded_traffic(w.name),
             "peak_source": peak_src + (" (bf16 x nominal dtype ratio)"
                                        if bound == "tensor" and NOMINAL_RATIO[w.kind] != 1.0 else ""),
             "algorithmic_bytes": workload_bytes(w), "algorithmic_flops": w.flops}
