@@ -28,16 +28,7 @@ namespace {
 
 std::atomic<uintptr_t> g_err_addr[kMaxDevices];
 
-unsigned int* err_word(int dev) {
-    uintptr_t a = g_err_addr[dev].load(std::memory_order_acquire);
-    if (a == 0) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_err_bs) != cudaSuccess) return nullptr;
-        a = reinterpret_cast<uintptr_t>(ptr);
-        g_err_addr[dev].store(a, std::memory_order_release);
-    }
-    return reinterpret_cast<unsigned int*>(a);
-}
+unsigned int* err_word(int dev) { return device_symbol(g_err_bs, g_err_addr, dev); }
 
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA, const void* B, const void* SFB,
@@ -89,11 +80,6 @@ gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const vo
     return run<CfgMxfp8>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
 }
 
-unsigned int read_clear_error_block_scaled() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_err_bs, sizeof(v)) != cudaSuccess) return 0;
-    if (v) cudaMemcpyToSymbol(g_err_bs, &zero, sizeof(zero));
-    return v;
-}
+unsigned int read_clear_error_block_scaled() { return read_clear_word(g_err_bs); }
 
 }  // namespace tn

@@ -30,16 +30,7 @@ namespace {
 
 std::atomic<uintptr_t> g_err_addr[kMaxDevices];
 
-unsigned int* err_word(int dev) {
-    uintptr_t a = g_err_addr[dev].load(std::memory_order_acquire);
-    if (a == 0) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_err_dense) != cudaSuccess) return nullptr;
-        a = reinterpret_cast<uintptr_t>(ptr);
-        g_err_addr[dev].store(a, std::memory_order_release);
-    }
-    return reinterpret_cast<unsigned int*>(a);
-}
+unsigned int* err_word(int dev) { return device_symbol(g_err_dense, g_err_addr, dev); }
 
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
@@ -108,11 +99,6 @@ gemm_status_t launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, co
     return dispatch<CfgE5m2Pair, CfgE5m2, CfgE5m2N128Pair, CfgE5m2N128>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
-unsigned int read_clear_error_dense() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_err_dense, sizeof(v)) != cudaSuccess) return 0;
-    if (v) cudaMemcpyToSymbol(g_err_dense, &zero, sizeof(zero));
-    return v;
-}
+unsigned int read_clear_error_dense() { return read_clear_word(g_err_dense); }
 
 }  // namespace tn

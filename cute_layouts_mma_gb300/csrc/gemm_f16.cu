@@ -34,16 +34,7 @@ namespace {
 
 std::atomic<uintptr_t> g_err_addr[kMaxDevices];
 
-unsigned int* err_word(int dev) {
-    uintptr_t a = g_err_addr[dev].load(std::memory_order_acquire);
-    if (a == 0) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_err_f16) != cudaSuccess) return nullptr;
-        a = reinterpret_cast<uintptr_t>(ptr);
-        g_err_addr[dev].store(a, std::memory_order_release);
-    }
-    return reinterpret_cast<unsigned int*>(a);
-}
+unsigned int* err_word(int dev) { return device_symbol(g_err_f16, g_err_addr, dev); }
 
 // Tensor maps and kernel parameters of one FP16 launch.
 template <class Cfg>
@@ -129,7 +120,7 @@ void* static_scratch(int dev) {
     uintptr_t a = g_static_scratch_addr[dev].load(std::memory_order_acquire);
     if (a == 0) {
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess) return nullptr;
         a = reinterpret_cast<uintptr_t>(ptr);
         g_static_scratch_addr[dev].store(a, std::memory_order_release);
     }
@@ -163,11 +154,6 @@ gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const voi
                                                        : run_noalloc<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
-unsigned int read_clear_error_f16() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_err_f16, sizeof(v)) != cudaSuccess) return 0;
-    if (v) cudaMemcpyToSymbol(g_err_f16, &zero, sizeof(zero));
-    return v;
-}
+unsigned int read_clear_error_f16() { return read_clear_word(g_err_f16); }
 
 }  // namespace tn

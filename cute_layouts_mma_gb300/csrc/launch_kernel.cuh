@@ -35,6 +35,29 @@ constexpr size_t sk_flag_bytes(int units) {
 // with the pool between calls; each call's block is returned on its stream).
 cudaMemPool_t scratch_pool(int dev);
 
+// Device address of a file-scope __device__ variable of the calling translation
+// unit on device `dev` (the current device), looked up once per device and kept in
+// `cache`; null if the lookup fails.
+template <class T>
+T* device_symbol(const T& symbol, std::atomic<uintptr_t> (&cache)[kMaxDevices], int dev) {
+    uintptr_t a = cache[dev].load(std::memory_order_acquire);
+    if (a == 0) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, symbol) != cudaSuccess) return nullptr;
+        a = reinterpret_cast<uintptr_t>(ptr);
+        cache[dev].store(a, std::memory_order_release);
+    }
+    return reinterpret_cast<T*>(a);
+}
+
+// Read a device error word of the current device and clear it if set (synchronous).
+inline unsigned int read_clear_word(const unsigned int& word) {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, word, sizeof(v)) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(word, &zero, sizeof(zero));
+    return v;
+}
+
 // Per-device, per-configuration launch state, set up on first use.
 template <class Cfg>
 struct LaunchState {
