@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import cute_layouts_mma_gb300 as tg
 
@@ -111,3 +112,17 @@ def test_valid_call_without_gpu_fails_cleanly():
         pytest.skip("a GPU is present")
     assert _f16(8, 8, 8) in (tg.GEMM_ERR_CUDA, tg.GEMM_ERR_UNSUPPORTED)
     assert _bs(8, 8, 256, tg.GEMM_FMT_NVFP4) in (tg.GEMM_ERR_CUDA, tg.GEMM_ERR_UNSUPPORTED)
+
+
+def test_python_wrappers_check_arguments_before_the_library():
+    # dtype, shape, device and layout checks happen in the binding (CPU tensors here)
+    A = torch.zeros(8, 16, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        tg.gemm_f16(A, A, None, torch.zeros(8, 8, dtype=torch.float16))       # not CUDA tensors
+    with pytest.raises(ValueError):
+        tg.gemm_bf16(A, A, None, torch.zeros(8, 8, dtype=torch.bfloat16))     # A is not bf16
+    with pytest.raises(ValueError):
+        tg.gemm_fp8(A.view(torch.uint8), A.view(torch.uint8), None, torch.zeros(8, 8), 5)  # unknown format
+    with pytest.raises(ValueError):
+        tg.gemm_block_scaled(A.view(torch.uint8), None, A.view(torch.uint8), None, None,
+                             torch.zeros(8, 8, dtype=torch.bfloat16), 7)       # unknown format

@@ -8,7 +8,9 @@ GEMM_ERR_TIMEOUT, the other CTA's tile is still computed exactly, and the CUDA
 context stays usable.
 
 The test build runs in a child process: two copies of the library (each with
-its own static CUDA runtime) cannot be used in one process.
+its own static CUDA runtime) cannot be used in one process.  The FP16 case has two
+single-CTA tiles; the NVFP4 case (two 128 x 128 tiles) also exercises the abandon
+path of the scale issuers and scale writers.
 """
 import json
 import os
@@ -40,15 +42,27 @@ CHILD = textwrap.dedent(r"""
     i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.gemm_f16.argtypes = [i64, i64, i64, vp, vp, vp, vp, ci, vp]
     lib.gemm_f16.restype = ci
+    lib.gemm_block_scaled.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, ci, vp]
+    lib.gemm_block_scaled.restype = ci
     lib.gemm_last_device_error.restype = ci
-    prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    kind = sys.argv[3]
     dev = torch.device("cuda", 0)
-    A, B = prob["A"].to(dev), prob["B"].to(dev)
-    D = torch.zeros(128, 512, dtype=torch.float16, device=dev)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    rc = lib.gemm_f16(128, 512, 256, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 0,
-                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if kind == "f16":
+        prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+        A, B = prob["A"].to(dev), prob["B"].to(dev)
+        D = torch.zeros(128, 512, dtype=torch.float16, device=dev)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        rc = lib.gemm_f16(128, 512, 256, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 0, stream)
+    else:
+        prob = inputs.make_problem("nvfp4", 128, 256, 512, seed=32, dist="int", with_c=False)
+        g = {k: prob[k].to(dev) for k in ("A", "SFA", "B", "SFB")}
+        D = torch.zeros(128, 256, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        rc = lib.gemm_block_scaled(128, 256, 512, g["A"].data_ptr(), g["SFA"].data_ptr(), g["B"].data_ptr(),
+                                   g["SFB"].data_ptr(), None, D.data_ptr(), 0, stream)
     status = lib.gemm_last_device_error()
     elapsed = time.time() - t0
     again = lib.gemm_last_device_error()
@@ -60,7 +74,12 @@ CHILD = textwrap.dedent(r"""
 """)
 
 
-def test_bounded_wait_runs_out_and_is_reported():
+# (kind, output columns computed by CTA 1, which the withheld stage does not affect)
+CASES = [("f16", slice(256, 512)), ("nvfp4", slice(128, 256))]
+
+
+@pytest.mark.parametrize("kind,cols", CASES, ids=[c[0] for c in CASES])
+def test_bounded_wait_runs_out_and_is_reported(kind, cols):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     with tempfile.TemporaryDirectory() as tmp:
@@ -68,7 +87,8 @@ def test_bounded_wait_runs_out_and_is_reported():
         out_npy = os.path.join(tmp, "d.npy")
         with open(script, "w") as f:
             f.write(CHILD)
-        r = subprocess.run([sys.executable, script, ROOT, out_npy], capture_output=True, text=True, timeout=600)
+        r = subprocess.run([sys.executable, script, ROOT, out_npy, kind], capture_output=True, text=True,
+                           timeout=600)
         assert r.returncode == 0, r.stderr[-2000:]
         res = json.loads(r.stdout.strip().splitlines()[-1])
         d_bits = np.load(out_npy).view(np.uint16)
@@ -77,9 +97,12 @@ def test_bounded_wait_runs_out_and_is_reported():
     assert 1.0 <= res["elapsed"] < 60.0          # the per-wait limit is 2 s
     assert res["again"] == tg.GEMM_OK            # the record is cleared once read
     assert res["usable"]
-    # CTA 1's tile (columns 256..511) was not affected: exact against the oracle
-    prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    # CTA 1's tile was not affected: exact against the oracle
+    if kind == "f16":
+        prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    else:
+        prob = inputs.make_problem("nvfp4", 128, 256, 512, seed=32, dist="int", with_c=False)
     d16, _ = P.oracle_result(prob)
-    assert np.array_equal(d_bits[:, 256:], d16[:, 256:])
+    assert np.array_equal(d_bits[:, cols], d16[:, cols])
     # and this process's product library is unaffected
     P.check(prob, P.run_gpu(prob), mode="exact")
