@@ -331,6 +331,15 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Accumulator columns c .. c+COLS-1 of this warp's 32 TMEM lanes into r (issue only;
+// the caller waits with tmem_ld_wait).
+template <int COLS>
+__device__ __forceinline__ void load_chunk(uint32_t tacc, int c, uint32_t* r) {
+    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(r));
+    if constexpr (COLS == 64)
+        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+}
+
 // One thread's share of an epilogue chunk: output row `row`, columns n .. n+COLS-1
 // of the tile, accumulator words r[0..COLS-1].  With kCStaged the warp's staging
 // buffer already holds the matching C chunk (TMA-loaded with the D tensor map's
@@ -805,10 +814,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll 1
                 for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
                     uint32_t r[EC];
-                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    if constexpr (EC == 64)
-                        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32),
-                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    load_chunk<EC>(tacc, c, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < EC / 4; ++j)
@@ -883,10 +889,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
                     if (n0 + c >= p.N) break;  // warp-uniform
                     uint32_t r[EC];
-                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    if constexpr (EC == 64)
-                        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32),
-                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    load_chunk<EC>(tacc, c, r);
                     tmem_ld_wait();
                     if (!rows_in) continue;
                     if constexpr (kSK) add_partials(r, b);
@@ -924,10 +927,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
                     if (n0 + c >= p.N) break;  // warp-uniform
                     uint32_t r[EC];
-                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    if constexpr (EC == 64)
-                        tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32),
-                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    load_chunk<EC>(tacc, c, r);
                     tmem_ld_wait();
                     if (!rows_in) continue;  // no row of this warp lies inside D
                     if constexpr (kSK) add_partials(r, b);
