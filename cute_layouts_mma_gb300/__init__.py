@@ -11,6 +11,7 @@ loaded, every call raises.
     gemm_fp8(A, B, C, D, fmt, stream=None)
     gemm_block_scaled(A, SFA, B, SFB, C, D, fmt, stream=None)
     gemm_status_string(code), gemm_last_device_error()
+    gemm(A, B, C=None, D=None, stream=None)   -- picks the call from A's dtype
 
 Tensors are torch CUDA tensors used only as device memory; `stream` is a
 torch.cuda.Stream (default: the current stream).
@@ -219,3 +220,28 @@ def gemm_block_scaled(A, SFA, B, SFB, C, D, fmt: int, stream=None) -> None:
 def gemm_last_device_error() -> int:
     """Synchronise the current device; GEMM_ERR_TIMEOUT if a kernel abandoned its work."""
     return lib().gemm_last_device_error()
+
+
+def gemm(A, B, C=None, D=None, stream=None, accum_dtype: int = GEMM_ACC_F32):
+    """D = A @ B^T + C, choosing the call from A's dtype: float16 -> gemm_f16 (fp16 D),
+    bfloat16 -> gemm_bf16, float8_e4m3fn / float8_e5m2 -> gemm_fp8 (bf16 D).  D is
+    allocated when not given; it is returned.  Block-scaled operands need their scale
+    tensors: use gemm_block_scaled for those."""
+    import torch
+    M, N = A.shape[0], B.shape[0]
+    kinds = {torch.float16: torch.float16, torch.bfloat16: torch.bfloat16,
+             torch.float8_e4m3fn: torch.bfloat16, torch.float8_e5m2: torch.bfloat16}
+    if A.dtype not in kinds:
+        raise ValueError(f"unsupported operand dtype {A.dtype}")
+    if D is None:
+        D = torch.empty(M, N, dtype=kinds[A.dtype], device=A.device)
+    if A.dtype == torch.float16:
+        gemm_f16(A, B, C, D, accum_dtype, stream)
+    elif A.dtype == torch.bfloat16:
+        gemm_bf16(A, B, C, D, stream)
+    else:
+        if B.dtype != A.dtype:
+            raise ValueError("A and B must have the same FP8 format")
+        gemm_fp8(A, B, C, D, GEMM_FP8_E4M3 if A.dtype == torch.float8_e4m3fn else GEMM_FP8_E5M2, stream)
+    return D
+

@@ -131,3 +131,16 @@ def test_concurrent_stream_k_calls_on_two_streams():
     assert tg.gemm_last_device_error() == tg.GEMM_OK
     for p, D in zip(probs, Ds):
         P.check(p, D.cpu(), rows=P.sample_rows(128, 16, seed=8), mode="exact")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float8_e4m3fn, torch.float8_e5m2])
+def test_gemm_dtype_dispatch(dtype):
+    kind = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float8_e4m3fn: "fp8e4m3",
+            torch.float8_e5m2: "fp8e5m2"}[dtype]
+    prob = inputs.make_problem(kind, 200, 264, 256, seed=71, dist="int" if kind.startswith("fp8") else "int2",
+                               with_c=True)
+    g = P.to_device(prob, P.device())
+    A, B = (g["A"].view(dtype), g["B"].view(dtype)) if kind.startswith("fp8") else (g["A"], g["B"])
+    D = tg.gemm(A, B, g["C"])
+    torch.cuda.synchronize()
+    P.check(prob, D.cpu(), mode="exact")
