@@ -45,7 +45,9 @@
 //                TCol = m // 32, byte = sfk) and writes them with tcgen05.st into
 //                its own 32 lanes -- the four quarters together replicate the
 //                tile to all four lane partitions -- then arrive on the leader's
-//                `sf_ready`.
+//                `full` barrier of the stage, so that the MMA issuer waits on one
+//                barrier per stage (a second wait per stage costs the single issuing
+//                thread ~200 cycles of its 512-cycle stage).
 // Every wait is bounded: past the limit the kernel records a timeout in the
 // device error word, makes the other warps give up, drains its in-flight copies
 // and MMAs, frees TMEM and returns.
@@ -203,15 +205,14 @@ struct Config {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;  // 1024-byte aligned
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-    // barriers: full[S], empty[S], sf_full[S], sf_ready[S], tmem_full[ACC], tmem_empty[ACC], drain,
+    // barriers: full[S], empty[S], sf_full[S], tmem_full[ACC], tmem_empty[ACC], drain,
     // c_load[EPI_WARPS][EPI_BUFS]
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = STAGES;
     static constexpr int BAR_SFFULL = 2 * STAGES;
-    static constexpr int BAR_SF = 3 * STAGES;
-    static constexpr int BAR_TFULL = 4 * STAGES;
-    static constexpr int BAR_TEMPTY = 4 * STAGES + ACC_BUFS;
-    static constexpr int BAR_DRAIN = 4 * STAGES + 2 * ACC_BUFS;
+    static constexpr int BAR_TFULL = 3 * STAGES;
+    static constexpr int BAR_TEMPTY = 3 * STAGES + ACC_BUFS;
+    static constexpr int BAR_DRAIN = 3 * STAGES + 2 * ACC_BUFS;
     static constexpr int BAR_CLOAD = BAR_DRAIN + 1;  // [epilogue warp][staging buffer]: C chunk landed
     static constexpr int NUM_BARS = BAR_CLOAD + EPI_WARPS * EPI_BUFS;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM base address, abort flag
@@ -472,10 +473,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar(Cfg::BAR_FULL + s), 2);    // the leader's A and B issuers
+            // the leader's A and B issuers, and (block-scaled) every scale-writer warp
+            mbar_init(bar(Cfg::BAR_FULL + s), 2 + (kBS ? 4 * PAIR : 0));
             mbar_init(bar(Cfg::BAR_EMPTY + s), 1);
             mbar_init(bar(Cfg::BAR_SFFULL + s), 2);  // SFA and SFB issuers
-            mbar_init(bar(Cfg::BAR_SF + s), 4 * PAIR);  // one arrival per scale-writer warp
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(bar(Cfg::BAR_TFULL + b), 1);
@@ -645,15 +646,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 for (int kb = k0; kb < k1; ++kb) {
                     const bool acc_kb = kb != k0;  // the first k block of a segment starts from 0
+                    // operands landed and (block-scaled) scales written to TMEM
                     if (!wait_bar<kPair>(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
                         ok = false;
                         break;
-                    }
-                    if constexpr (kBS) {
-                        if (!wait_bar<kPair>(bar(Cfg::BAR_SF + s), ph, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
                     }
                     tc_fence_after_sync();
                     const uint64_t adesc = adesc0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
@@ -754,9 +750,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         // The scales are TMEM data whose writes tcgen05.wait::st has
                         // completed: the leader needs no release of generic memory.
                         if constexpr (kPair)
-                            mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_SF + s));
+                            mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_FULL + s));
                         else
-                            mbar_arrive(bar(Cfg::BAR_SF + s));
+                            mbar_arrive(bar(Cfg::BAR_FULL + s));
                     }
                     if (++s == STAGES) {
                         s = 0;
