@@ -646,8 +646,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 for (int kb = k0; kb < k1; ++kb) {
                     const bool acc_kb = kb != k0;  // the first k block of a segment starts from 0
-                    // operands landed and (block-scaled) scales written to TMEM
-                    if (!wait_bar<kPair>(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
+                    // Operands landed and (block-scaled) scales written to TMEM.  The dense
+                    // kinds' barrier completes through the arrivals of this CTA's issuers and
+                    // the transaction bytes of both CTAs' copies, so a CTA-scope wait
+                    // suffices (a cluster-scope acquire costs the issuing thread ~4% of the
+                    // stage); the scale writers of the peer CTA arrive with cluster scope.
+                    if (!wait_bar<kPair && kBS>(bar(Cfg::BAR_FULL + s), ph, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
