@@ -162,7 +162,7 @@ struct Config {
     static constexpr int EPI_BUFS = EPI_BUFS_;
     // Stream-K needs fp32 accumulation (partials are fp32 sums); the 8-epilogue-warp
     // configuration has no registers to spare for it and stays data-parallel.
-    static constexpr bool kStreamK = KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4;
+    static constexpr bool kStreamK = KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4 && !(EPI_BUFS_ == 1 && 2 * EPI_COLS_ == BN_);
     static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
     // 4 epilogue warps (warps 4-7), or 8 (also warps 13-16): two per TMEM lane
@@ -176,6 +176,12 @@ struct Config {
     // Staging covers a warp's whole 32-row slice of the tile: the accumulator is
     // drained to shared memory and released before any store is issued.
     static constexpr bool kWholeTileStaging = EPI_COLS * EPI_BUFS == BN / EPI_SPLIT;
+    // Or: one staging buffer, two chunks per warp, no C.  The first chunk is staged,
+    // the second is rounded and held in registers when the accumulator is released,
+    // and staged once the first chunk's store has read the buffer: half the staging
+    // memory of whole-slice staging, with the same early release.  Launched only
+    // without C (the launcher picks a whole-slice instance when C is given).
+    static constexpr bool kHoldLastChunk = EPI_BUFS == 1 && 2 * EPI_COLS == BN / EPI_SPLIT;
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
@@ -364,6 +370,26 @@ __device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int
         }
         *slot = pack8<KIND>(f);
     }
+}
+
+// Accumulator words r[0..COLS-1] rounded to COLS / 8 output vectors (no C).
+template <int KIND, int COLS>
+__device__ __forceinline__ void pack_chunk(const uint32_t* r, uint4* out) {
+#pragma unroll
+    for (int v = 0; v < COLS / 8; ++v) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
+        out[v] = pack8<KIND>(f);
+    }
+}
+
+// Output vectors of one row into a swizzled staging buffer (the layout stage_chunk writes).
+template <int COLS>
+__device__ __forceinline__ void stage_packed(const uint4* pk, uint8_t* buf, int lane) {
+#pragma unroll
+    for (int v = 0; v < COLS / 8; ++v)
+        *reinterpret_cast<uint4*>(buf + layout::swizzled_offset(COLS * 2, lane, 16 * v)) = pk[v];
 }
 
 // Scale-factor writer for one TMEM lane quarter.  The stage's scale boxes sit in
@@ -873,6 +899,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         for (int c = c_begin, b = 0; c < c_end && n0 + c < p.N; c += EC, ++b) load_c(b, n0 + c, m_warp);
                 }
                 __syncwarp();
+            } else if constexpr (Cfg::kHoldLastChunk) {
+                if (rows_in && lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores have read the buffer
+                __syncwarp();
             } else if (has_c && rows_in && lane == 0 && n0 + c_begin < p.N) {
                 bulk_wait_group_read<EB - 1>();
                 load_c(eb, n0 + c_begin, m_warp);
@@ -920,6 +949,56 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         for (int c = c_begin, b = 0; c < c_end && n0 + c < p.N; c += EC, ++b)
                             tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
                         bulk_commit_group();
+                    }
+                }
+            } else if constexpr (Cfg::kHoldLastChunk) {
+                // Chunk 0 to the staging buffer, chunk 1 rounded into registers; release
+                // the accumulator; store chunk 0, then stage and store chunk 1 (no C).
+                static_assert(!kSK, "whole tiles only");
+                const int c1 = c_begin + EC;
+                const bool have0 = n0 + c_begin < p.N;  // warp-uniform
+                const bool have1 = n0 + c1 < p.N;
+                uint4 pk1[EC / 8];
+                if (have0) {
+                    uint32_t r[EC];
+                    load_chunk<EC>(tacc, c_begin, r);
+                    tmem_ld_wait();
+                    if (rows_in) stage_chunk<KIND, EC, false>(r, stg, lane);
+                }
+                if (have1) {
+#pragma unroll
+                    for (int h = 0; h < EC / 32; ++h) {  // 32 columns at a time: fewer live registers
+                        uint32_t r[32];
+                        load_chunk<32>(tacc, c1 + 32 * h, r);
+                        tmem_ld_wait();
+                        pack_chunk<KIND, 32>(r, pk1 + 4 * h);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                    else
+                        mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+                }
+                if (rows_in && have0) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmD, stg_u32, n0 + c_begin, m_warp);
+                        bulk_commit_group();
+                    }
+                    if (have1) {
+                        if (lane == 0) bulk_wait_group_read<0>();  // chunk 0's store has read the buffer
+                        __syncwarp();
+                        stage_packed<EC>(pk1, stg, lane);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmD, stg_u32, n0 + c1, m_warp);
+                            bulk_commit_group();
+                        }
                     }
                 }
             } else {

@@ -141,9 +141,11 @@ def test_nvfp4_integers_bit_exact(with_c):
     P.check(prob, P.run_gpu(prob), mode="exact")
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 264, 768), (129, 8, 256), (384, 1024, 2048)])
-def test_nvfp4_random_tolerance(M, N, K):
-    prob = inputs.make_problem("nvfp4", M, N, K, seed=M + K, dist="codes", with_c=True)
+@pytest.mark.parametrize("with_c", [True, False])
+@pytest.mark.parametrize("M,N,K", [(200, 264, 768), (129, 8, 256), (384, 1024, 2048), (520, 200, 512)])
+def test_nvfp4_random_tolerance(M, N, K, with_c):
+    # M > 128 without C runs the instance that holds half of each slice in registers
+    prob = inputs.make_problem("nvfp4", M, N, K, seed=M + K, dist="codes", with_c=with_c)
     P.check(prob, P.run_gpu(prob), mode="tol")
 
 
