@@ -36,6 +36,60 @@ std::atomic<uintptr_t> g_err_addr[kMaxDevices];
 
 unsigned int* err_word(int dev) { return device_symbol(g_err_bs, g_err_addr, dev); }
 
+// One scale matrix to regroup: src [rows][cols16 * 16] bytes, row-major; dst
+// [groups][cols16][128][16], rows at or past `rows` zero.
+struct PackJob {
+    const uint8_t* src;
+    uint8_t* dst;
+    int rows;
+    int groups;
+};
+
+// Regroups SFA and SFB into the packed blocks the NVFP4 stages load (one warp per
+// 2 KB block: lane l moves rows l, l+32, l+64, l+96 of the block, so each store
+// instruction writes 512 contiguous bytes).  A block holds exactly the bytes of the
+// 16-byte x 128-row scale box of one stage, in the same row-major order.
+__global__ void __launch_bounds__(256) pack_scales_kernel(PackJob a, PackJob b, int cols16) {
+    griddep_wait();  // the scales may be written by the previous launch on the stream
+    griddep_launch_dependents();
+    const int w = static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int blocks_a = a.groups * cols16;
+    if (w >= blocks_a + b.groups * cols16) return;
+    const PackJob& j = w < blocks_a ? a : b;
+    const int blk = w < blocks_a ? w : w - blocks_a;
+    const int g = blk / cols16, c = blk - g * cols16;
+    const size_t pitch = static_cast<size_t>(cols16) * 16;
+    uint4* out = reinterpret_cast<uint4*>(j.dst + static_cast<size_t>(blk) * 2048);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 32 * i + lane;
+        const int row = g * 128 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < j.rows) v = __ldg(reinterpret_cast<const uint4*>(j.src + static_cast<size_t>(row) * pitch + 16 * c));
+        out[r] = v;
+    }
+}
+
+// Enqueue the regrouping of SFA (ga row groups) and SFB (gb) into `packed` on `stream`.
+cudaError_t launch_pack(const void* SFA, int64_t M, int ga, const void* SFB, int64_t N, int gb, int cols16,
+                        uint8_t* packed, cudaStream_t stream) {
+    const PackJob a{static_cast<const uint8_t*>(SFA), packed, static_cast<int>(M), ga};
+    const PackJob b{static_cast<const uint8_t*>(SFB), packed + static_cast<size_t>(ga) * cols16 * 2048,
+                    static_cast<int>(N), gb};
+    const long long warps = static_cast<long long>(ga + gb) * cols16;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pack_scales_kernel, a, b, cols16);
+}
+
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA, const void* B, const void* SFB,
                   const void* C, void* D, cudaStream_t stream, int sms, int dev) {
@@ -45,16 +99,21 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
     const int64_t sf_cols = K / (fp4 ? 16 : 32);  // scale bytes per row
     CUtensorMap ta, tb, tsa, tsb, td, tc;
     // Data boxes: 128 bytes of K (256 E2M1 / 128 E4M3 elements) x rows, 128B swizzle;
-    // A boxes are this CTA's 128 rows, B boxes its BN/PAIR rows.  Scale boxes: 16 bytes
-    // (16 scale blocks) x rows, no swizzle: 128 SFA rows, all BN SFB rows of the tile.
-    // D: bf16 [M][N], stored in 32-row x EPI_COLS boxes from the epilogue staging.
+    // A boxes are this CTA's 128 rows, B boxes its BN/PAIR rows.  Scale boxes (MXFP8):
+    // 16 bytes (16 scale blocks) x rows, no swizzle: 128 SFA rows, all BN SFB rows of
+    // the tile.  D: bf16 [M][N], stored in 32-row x EPI_COLS boxes from the staging.
     if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, M, row_bytes, 128, Cfg::BM, 128) ||
         !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, N, row_bytes, 128, Cfg::BN_CTA, 128) ||
-        !encode_tma_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, sf_cols, M, sf_cols, 16, Cfg::BM, 0) ||
-        !encode_tma_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, sf_cols, N, sf_cols, 16, Cfg::BN, 0) ||
         !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
                        Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;
+    if constexpr (Cfg::kPackedScales) {
+        tsa = ta;  // unused: the scales arrive as packed blocks
+        tsb = ta;
+    } else if (!encode_tma_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, sf_cols, M, sf_cols, 16, Cfg::BM, 0) ||
+               !encode_tma_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, sf_cols, N, sf_cols, 16, Cfg::BN, 0)) {
+        return GEMM_ERR_CUDA;
+    }
     // C (if any): the same boxes as D, TMA-loaded into the epilogue staging buffers.
     if (C == nullptr)
         tc = td;
@@ -62,7 +121,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
         return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (err == nullptr) return GEMM_ERR_CUDA;
-    Params p;
+    Params p{};
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -72,7 +131,26 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
     p.C = C;
     p.D = D;
     p.err = err;
-    if (launch_config<Cfg>(ta, tb, tsa, tsb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if constexpr (Cfg::kPackedScales) {
+        // Packed scales for this call, taken from the device's stream-ordered pool and
+        // returned on the same stream after the GEMM.  Row groups cover whole tiles.
+        const int cols16 = static_cast<int>(sf_cols / 16);
+        const int ga = p.num_m_blocks * (Cfg::BM_TILE / 128);
+        const int gb = p.num_n_blocks * Cfg::SFB_GROUPS;
+        void* packed = nullptr;
+        if (cudaMallocFromPoolAsync(&packed, (static_cast<size_t>(ga) + gb) * cols16 * 2048, scratch_pool(dev),
+                                    stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        p.sfa_packed = static_cast<const uint8_t*>(packed);
+        p.sfb_packed = static_cast<const uint8_t*>(packed) + static_cast<size_t>(ga) * cols16 * 2048;
+        p.sf_cols16 = cols16;
+        cudaError_t e = launch_pack(SFA, M, ga, SFB, N, gb, cols16, static_cast<uint8_t*>(packed), stream);
+        if (e == cudaSuccess) e = launch_config<Cfg>(ta, tb, tsa, tsb, td, tc, p, sms, dev, stream);
+        const cudaError_t f = cudaFreeAsync(packed, stream);
+        if (e != cudaSuccess || f != cudaSuccess) return GEMM_ERR_CUDA;
+    } else if (launch_config<Cfg>(ta, tb, tsa, tsb, td, tc, p, sms, dev, stream) != cudaSuccess) {
+        return GEMM_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

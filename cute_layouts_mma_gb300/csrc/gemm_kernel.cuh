@@ -24,8 +24,9 @@
 //                peer's copies signal the leader's barrier directly).  A TMA
 //                instruction occupies its issuing warp for a few hundred cycles
 //                whatever the box size, so each operand stream has its own warp.
-//   warps 3, 12  (block-scaled only) TMA issuers of the raw scale boxes (this
-//                CTA's 128 SFA rows, all BN SFB rows of the tile) on `sf_full`.
+//   warps 3, 12  (block-scaled only) issuers of the raw scale boxes (this CTA's
+//                128 SFA rows, all BN SFB rows of the tile) on `sf_full`: TMA boxes
+//                of the row-major scales, or (NVFP4) bulk copies of packed blocks.
 //   warp 1       TMEM allocation; in the leader, the MMA issuer (one thread):
 //                tcgen05.mma into a TMEM accumulator, 32 bytes of K per MMA;
 //                tcgen05.commit frees the stage (`empty`, in both CTAs) and, at the
@@ -100,6 +101,13 @@ struct Params {
     long long sk_total;    // sk_tiles * num_k_blocks
     float* ws;             // partials: [unit][rank][epilogue warp][chunk][col/4][lane][4]
     unsigned int* flags;   // [unit][rank][epilogue warp]: 1 once that partial is written
+    // Block-scaled kinds with packed scales (Config::kPackedScales): SFA and SFB
+    // regrouped into contiguous 2 KB blocks [row group of 128][16-byte scale column]
+    // [128 rows][16 bytes] (rows past the matrix are zero), so that one stage's
+    // scales of 128 rows arrive in one bulk copy instead of 128 strided 16-byte rows.
+    const uint8_t* sfa_packed;
+    const uint8_t* sfb_packed;
+    int sf_cols16;  // 16-byte scale columns per row (blocks per row group)
 };
 
 enum SegKind : int { SEG_FULL = 0, SEG_PARTIAL = 1, SEG_OWNER = 2 };
@@ -184,6 +192,9 @@ struct Config {
     static constexpr bool kHoldLastChunk = EPI_BUFS == 1 && 2 * EPI_COLS == BN / EPI_SPLIT;
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
+    // NVFP4 stages read their scales from packed 2 KB blocks (one bulk copy per 128
+    // rows); MXFP8, whose 16-byte scale box serves four stages, keeps the TMA boxes.
+    static constexpr bool kPackedScales = KIND == KIND_NVFP4;
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
     // writers, 12 SFB issuer, 13-16 second epilogue set
     static constexpr int THREADS = EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256);
@@ -518,7 +529,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
         if (p.C != nullptr) tma_prefetch_desc(&tmC);
-        if constexpr (kBS) {
+        if constexpr (kBS && !Cfg::kPackedScales) {
             tma_prefetch_desc(&tmSFA);
             tma_prefetch_desc(&tmSFB);
         }
@@ -602,7 +613,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // MXFP8 uses 4 of them (so the same box serves 4 stages).
                     const int sfx = (KIND == KIND_NVFP4) ? kb * 16 : (kb >> 2) * 16;
                     const uint32_t sb = bar(Cfg::BAR_SFFULL + s);
-                    if (role == 2) {
+                    if constexpr (Cfg::kPackedScales) {
+                        // block (row group, 16-byte column kb): the same bytes the box holds
+                        const size_t cols = static_cast<size_t>(p.sf_cols16);
+                        if (role == 2) {
+                            mbar_arrive_expect_tx(sb, Cfg::BM * 16);
+                            bulk_load(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
+                                      p.sfa_packed + ((m0 >> 7) * cols + kb) * 2048, 2048, sb);
+                        } else {
+                            mbar_arrive_expect_tx(sb, Cfg::SFB_GROUPS * 2048);
+#pragma unroll
+                            for (int g = 0; g < Cfg::SFB_GROUPS; ++g)
+                                bulk_load(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + g * 2048,
+                                          p.sfb_packed + (((nb0 >> 7) + g) * cols + kb) * 2048, 2048, sb);
+                        }
+                    } else if (role == 2) {
                         mbar_arrive_expect_tx(sb, Cfg::BM * 16);
                         tma_load_2d(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, &tmSFA, sb, sfx, m0);
                     } else {

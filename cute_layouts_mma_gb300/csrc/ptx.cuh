@@ -81,6 +81,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Contiguous (non-tensor) bulk copy global -> this CTA's shared memory, completion
+// signalled on `bar` as transaction bytes.  Both addresses 16-byte aligned, `bytes`
+// a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk async-group completion).
 // The box is clipped to the tensor: rows/columns outside it are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {

@@ -23,7 +23,11 @@
  *     19.5 MB on 152 SMs) is taken with cudaMallocFromPoolAsync on `stream`
  *     from a per-device memory pool the library creates on first need, and
  *     returned to the pool with cudaFreeAsync on `stream` after the kernel; the
- *     pool keeps its memory for later calls until the process exits.  A failed
+ *     pool keeps its memory for later calls until the process exits.  NVFP4
+ *     calls of gemm_block_scaled also take, from the same pool and for the same
+ *     duration, a copy of SFA and SFB regrouped into contiguous 2 KB blocks (one
+ *     per 128 rows and 16 scale bytes; about the size of SFA plus SFB), written
+ *     by a small kernel launched on `stream` before the GEMM.  A failed
  *     allocation returns GEMM_ERR_CUDA and launches nothing.
  *   - Matrices are dense and row-major with no padding: A rows are K elements
  *     long (NVFP4: K/2 bytes), B rows likewise, C and D rows are N elements.
