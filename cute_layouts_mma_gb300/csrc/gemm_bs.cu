@@ -16,6 +16,7 @@ namespace tn {
 // buffer, so the staging takes 32 KB instead of 64.
 using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 2, 2, 8>;
 using CfgNvfp4PairNoC = Config<KIND_NVFP4, 256, 5, 1, 64, 1, 2, 8>;
+using CfgNvfp4PairReg = Config<KIND_NVFP4, 256, 5, 1, 64, 1, 2, 8, 128, true>;
 // NVFP4, single CTAs (M <= 128): 128 x 128 tiles, 5 stages, two TMEM accumulators
 // (2 x 128 + 5 x 32 scale columns), each epilogue warp staging its whole 32 x 128
 // slice.  Measured 1.2-1.75x faster than 128 x 256 tiles with one accumulator on
@@ -161,8 +162,7 @@ gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const vo
                                        cudaStream_t stream, int sms, int dev) {
     if (fmt == GEMM_FMT_NVFP4)
         return M <= 128      ? run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
-               : C == nullptr ? run<CfgNvfp4PairNoC>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
-                              : run<CfgNvfp4Pair>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
+                             : run<CfgNvfp4PairReg>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
     return run<CfgMxfp8>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
 }
 

@@ -154,7 +154,7 @@ __device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it
 }
 
 template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
-          int EPI_WARPS_ = 4, int ROW_BYTES_ = 128>
+          int EPI_WARPS_ = 4, int ROW_BYTES_ = 128, bool REG_DRAIN_ = false>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
@@ -170,7 +170,8 @@ struct Config {
     static constexpr int EPI_BUFS = EPI_BUFS_;
     // Stream-K needs fp32 accumulation (partials are fp32 sums); the 8-epilogue-warp
     // configuration has no registers to spare for it and stays data-parallel.
-    static constexpr bool kStreamK = KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4 && !(EPI_BUFS_ == 1 && 2 * EPI_COLS_ == BN_);
+    static constexpr bool kStreamK =
+        KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4 && !(EPI_BUFS_ == 1 && 2 * EPI_COLS_ == BN_) && !REG_DRAIN_;
     static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
     // 4 epilogue warps (warps 4-7), or 8 (also warps 13-16): two per TMEM lane
@@ -189,15 +190,29 @@ struct Config {
     // and staged once the first chunk's store has read the buffer: half the staging
     // memory of whole-slice staging, with the same early release.  Launched only
     // without C (the launcher picks a whole-slice instance when C is given).
-    static constexpr bool kHoldLastChunk = EPI_BUFS == 1 && 2 * EPI_COLS == BN / EPI_SPLIT;
+    static constexpr bool kHoldLastChunk = !REG_DRAIN_ && EPI_BUFS == 1 && 2 * EPI_COLS == BN / EPI_SPLIT;
+    // Register drain (block-scaled pairs, 8 epilogue warps, 512 threads = 4 warpgroups):
+    // the issuers / MMA warpgroup and the scale writers give up registers
+    // (setmaxnreg) so that each epilogue warp takes its whole 32 x 128 slice of the
+    // accumulator into registers with one TMEM round trip and releases it at once;
+    // rounding, staging (one 64-column buffer) and stores follow.
+    static constexpr bool kRegDrain = REG_DRAIN_;
+    static_assert(!kRegDrain || (EPI_WARPS_ == 8 && EPI_BUFS_ == 1 && 2 * EPI_COLS_ * 2 == BN_),
+                  "register drain: 8 epilogue warps, two 64-column chunks per warp, one staging buffer");
+    // Registers per thread of each warpgroup under kRegDrain (launched with 128):
+    // issuers and MMA, epilogue, scale writers, epilogue.  They add up to 4 x 128.
+    static constexpr int kRegsIssue = 48, kRegsEpi = 184, kRegsWriter = 96;
+    static_assert(kRegsIssue + kRegsWriter + 2 * kRegsEpi == 4 * 128, "register split adds up to the launch's");
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
     // NVFP4 stages read their scales from packed 2 KB blocks (one bulk copy per 128
     // rows); MXFP8, whose 16-byte scale box serves four stages, keeps the TMA boxes.
     static constexpr bool kPackedScales = KIND == KIND_NVFP4;
+    static_assert(!kRegDrain || kPackedScales, "register drain: NVFP4 (one scale issuer warp)");
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
-    // writers, 12 SFB issuer, 13-16 second epilogue set
-    static constexpr int THREADS = EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256);
+    // writers, 12 SFB issuer, 13-16 second epilogue set; with kRegDrain warp 3 issues
+    // both scale streams and warps 12-15 are the second epilogue set.
+    static constexpr int THREADS = kRegDrain ? 512 : (EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256));
     // Bytes of K per operand row and stage: 128 (the 128-byte swizzle), or 64 / 32 for
     // problems whose whole K is narrower ("数据布局及其记号", swizzle section: the same
     // hierarchy with 8 x 64-byte and 8 x 32-byte atoms).  32 bytes of K per MMA.
@@ -620,7 +635,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             mbar_arrive_expect_tx(sb, Cfg::BM * 16);
                             bulk_load(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
                                       p.sfa_packed + ((m0 >> 7) * cols + kb) * 2048, 2048, sb);
-                        } else {
+                        }
+                        if (role == 3 || Cfg::kRegDrain) {  // kRegDrain: one warp issues both
                             mbar_arrive_expect_tx(sb, Cfg::SFB_GROUPS * 2048);
 #pragma unroll
                             for (int g = 0; g < Cfg::SFB_GROUPS; ++g)
@@ -669,9 +685,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
     };
 
-    if (warp == 0 || warp == 2 || (kBS && (warp == 3 || warp == 12))) {
-        if (lane == 0) issue_loop(warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : 3);
-    } else if (warp == 1) {
+    // ------------------------------------------------------------------ roles
+    auto mma_role = [&]() {
         if (lane == 0 && leader) {
             // ---------------------------------------------------------- MMA issuer
             // One thread issues every MMA; each tcgen05 instruction costs it tens of
@@ -780,7 +795,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 wait_bar_drain(bar(Cfg::BAR_DRAIN), 0u);
             }
         }
-    } else if (warp >= 8 && warp < 12) {
+    };
+    auto writer_role = [&]() {
         if constexpr (kBS) {
             // -------------------------------------------------------------- scale writers
             const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -816,12 +832,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
         }
-    } else if ((warp >= 4 && warp < 8) || (Cfg::EPI_WARPS == 8 && warp >= 13 && warp < 17)) {
+    };
+    auto epilogue_role = [&]() {
         // -------------------------------------------------------------- epilogue
         constexpr int EC = Cfg::EPI_COLS;
         constexpr int EB = Cfg::EPI_BUFS;
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
-        const int e = warp < 8 ? warp - 4 : warp - 9;  // epilogue warp index
+        const int e = warp < 8 ? warp - 4 : (Cfg::kRegDrain ? warp - 8 : warp - 9);  // epilogue warp index
         const int c_begin = (e >> 2) * Cfg::BN_EPI;    // this warp's columns of the tile
         const int c_end = c_begin + Cfg::BN_EPI;
         uint8_t* stg = smem + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
@@ -927,6 +944,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             } else if constexpr (Cfg::kHoldLastChunk) {
                 if (rows_in && lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores have read the buffer
                 __syncwarp();
+            } else if constexpr (Cfg::kRegDrain) {
+                if (rows_in && lane == 0) {
+                    bulk_wait_group_read<0>();  // the previous tile's stores have read the buffer
+                    if (has_c && n0 + c_begin < p.N) load_c(0, n0 + c_begin, m_warp);
+                }
+                __syncwarp();
             } else if (has_c && rows_in && lane == 0 && n0 + c_begin < p.N) {
                 bulk_wait_group_read<EB - 1>();
                 load_c(eb, n0 + c_begin, m_warp);
@@ -975,6 +998,56 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
                         bulk_commit_group();
                     }
+                }
+            } else if constexpr (Cfg::kRegDrain) {
+                // The warp's whole slice (BN_EPI fp32 columns) into registers with one
+                // wait, release the accumulator, then per 64-column chunk: (C added from
+                // the staging buffer) round, stage, TMA-store.
+                static_assert(!kSK, "whole tiles only");
+                uint32_t r[Cfg::BN_EPI];
+#pragma unroll
+                for (int h = 0; h < Cfg::BN_EPI / 32; ++h)
+                    tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c_begin + 32 * h),
+                                       *reinterpret_cast<uint32_t(*)[32]>(r + 32 * h));
+                tmem_ld_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                    else
+                        mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
+                }
+                if (rows_in) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::BN_EPI / EC; ++j) {
+                        const int c = c_begin + j * EC;
+                        if (n0 + c >= p.N) break;  // warp-uniform
+                        if (j > 0) {
+                            if (lane == 0) {
+                                bulk_wait_group_read<0>();  // the previous chunk's store has read the buffer
+                                if (has_c) load_c(0, n0 + c, m_warp);
+                            }
+                            __syncwarp();
+                        }
+                        if (has_c) {
+                            ok = __all_sync(0xffffffffu,
+                                            wait_bar(bar(Cfg::BAR_CLOAD + e * EB), cph & 1u, abort_flag, p.err));
+                            cph ^= 1u;
+                            cpending = 0;
+                            if (!ok) break;
+                            stage_chunk<KIND, EC, true>(r + j * EC, stg, lane);
+                        } else {
+                            stage_chunk<KIND, EC, false>(r + j * EC, stg, lane);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmD, stg_u32, n0 + c, m_warp);
+                            bulk_commit_group();
+                        }
+                    }
+                    if (!ok) break;
                 }
             } else if constexpr (Cfg::kHoldLastChunk) {
                 // Chunk 0 to the staging buffer, chunk 1 rounded into registers; release
@@ -1083,6 +1156,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             bulk_wait_group_all();
         }
         __syncwarp();
+    };
+    if constexpr (Cfg::kRegDrain) {
+        // Each warpgroup sets its register budget inside its own branch (all four
+        // warps execute the same setmaxnreg, and the code after it is compiled to
+        // that budget): issuers and MMA, then the scale writers, release registers;
+        // the two epilogue warpgroups take them.
+        const int wg = warp >> 2;
+        if (wg == 0) {
+            setmaxnreg_dec<Cfg::kRegsIssue>();
+            if (warp == 1)
+                mma_role();
+            else if (lane == 0)
+                issue_loop(warp == 0 ? 0 : warp == 2 ? 1 : 2);
+        } else if (wg == 2) {
+            setmaxnreg_dec<Cfg::kRegsWriter>();
+            writer_role();
+        } else {
+            setmaxnreg_inc<Cfg::kRegsEpi>();
+            epilogue_role();
+        }
+    } else if (warp == 0 || warp == 2 || (kBS && (warp == 3 || warp == 12))) {
+        if (lane == 0) issue_loop(warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : 3);
+    } else if (warp == 1) {
+        mma_role();
+    } else if (warp >= 8 && warp < 12) {
+        writer_role();
+    } else if ((warp >= 4 && warp < 8) || (Cfg::EPI_WARPS == 8 && warp >= 13 && warp < 17)) {
+        epilogue_role();
     }
 
     tc_fence_before_sync();

@@ -123,6 +123,15 @@ cudaError_t prepare_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[
     if (units == 0) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        if constexpr (Cfg::kRegDrain) {
+            // The warpgroups' register increases are met only by the decreases and the
+            // launch's own allocation: the kernel must be launched with 128 registers
+            // per thread (512 threads x 128 = the SM's 65536), or they would wait forever.
+            cudaFuncAttributes fa{};
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != 128 || Cfg::THREADS * 128 != 65536) return cudaErrorInvalidConfiguration;
+        }
         units = sms;
         if (Cfg::PAIR == 2) {
             cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
