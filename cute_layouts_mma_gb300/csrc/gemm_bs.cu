@@ -6,17 +6,14 @@
 
 namespace tn {
 
-// NVFP4, CTA pairs (M > 128): 256 x 256 tiles, one TMEM accumulator (256
-// columns; the scale slots, 48 columns per stage, use the rest) and 8 epilogue
-// warps, each draining a 32 x 128 slice, so the accumulator is released before
-// any store is issued.  With C: 4 stages, each warp staging its whole slice
-// (C is TMA-loaded into the staging ahead of the accumulator).  Without C: 5
-// stages; each warp stages the first 64-column chunk of its slice and holds the
-// second, rounded, in registers until the first chunk's store has read the
-// buffer, so the staging takes 32 KB instead of 64.
-using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 4, 1, 64, 2, 2, 8>;
-using CfgNvfp4PairNoC = Config<KIND_NVFP4, 256, 5, 1, 64, 1, 2, 8>;
-using CfgNvfp4PairReg = Config<KIND_NVFP4, 256, 5, 1, 64, 1, 2, 8, 128, true>;
+// NVFP4, CTA pairs (M > 128): 256 x 256 tiles, 5 stages, one TMEM accumulator
+// (256 columns; the scale slots, 5 x 48 columns, use the rest).  512 threads in
+// four warpgroups: issuers and MMA, epilogue, scale writers, epilogue.  The first
+// and third give registers to the epilogue warpgroups (setmaxnreg), so each of the
+// 8 epilogue warps takes its whole 32 x 128 slice of the accumulator into
+// registers with one TMEM round trip and releases it before rounding, staging
+// (one 64-column buffer per warp; C TMA-loaded into it) and storing.
+using CfgNvfp4Pair = Config<KIND_NVFP4, 256, 5, 1, 64, 1, 2, 8, 128, true>;
 // NVFP4, single CTAs (M <= 128): 128 x 128 tiles, 5 stages, two TMEM accumulators
 // (2 x 128 + 5 x 32 scale columns), each epilogue warp staging its whole 32 x 128
 // slice.  Measured 1.2-1.75x faster than 128 x 256 tiles with one accumulator on
@@ -94,7 +91,6 @@ cudaError_t launch_pack(const void* SFA, int64_t M, int ga, const void* SFB, int
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA, const void* B, const void* SFB,
                   const void* C, void* D, cudaStream_t stream, int sms, int dev) {
-    if (Cfg::kHoldLastChunk && C != nullptr) return GEMM_ERR_UNSUPPORTED;  // not dispatched with C
     constexpr bool fp4 = Cfg::KIND == KIND_NVFP4;
     const int64_t row_bytes = fp4 ? K / 2 : K;    // data bytes per row
     const int64_t sf_cols = K / (fp4 ? 16 : 32);  // scale bytes per row
@@ -162,7 +158,7 @@ gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const vo
                                        cudaStream_t stream, int sms, int dev) {
     if (fmt == GEMM_FMT_NVFP4)
         return M <= 128      ? run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
-                             : run<CfgNvfp4PairReg>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
+                             : run<CfgNvfp4Pair>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
     return run<CfgMxfp8>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);
 }
 

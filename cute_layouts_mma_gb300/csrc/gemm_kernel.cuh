@@ -27,12 +27,13 @@
 //   warps 3, 12  (block-scaled only) issuers of the raw scale boxes (this CTA's
 //                128 SFA rows, all BN SFB rows of the tile) on `sf_full`: TMA boxes
 //                of the row-major scales, or (NVFP4) bulk copies of packed blocks.
+//                In the register-drain layout warp 3 issues both.
 //   warp 1       TMEM allocation; in the leader, the MMA issuer (one thread):
 //                tcgen05.mma into a TMEM accumulator, 32 bytes of K per MMA;
 //                tcgen05.commit frees the stage (`empty`, in both CTAs) and, at the
 //                end of a tile, hands the accumulator to the epilogues
 //                (`tmem_full`, in both CTAs).
-//   warps 4-7    epilogue (and 13-16 in the 8-epilogue-warp instance): tcgen05.ld
+//   warps 4-7    epilogue (and 12-15 in the register-drain layout): tcgen05.ld
 //                of the accumulator (warp w reads TMEM lanes 32*(w%4) .. +31, i.e.
 //                rows of the tile), adds any stream-K partials and C in fp32, rounds
 //                once to fp16 / bf16, writes the 32-row chunk to a swizzled
@@ -49,6 +50,10 @@
 //                `full` barrier of the stage, so that the MMA issuer waits on one
 //                barrier per stage (a second wait per stage costs the single issuing
 //                thread ~200 cycles of its 512-cycle stage).
+// Register-drain layout (NVFP4 CTA pairs): 512 threads, four warpgroups -- 0-3
+// issuers and MMA, 4-7 epilogue, 8-11 scale writers, 12-15 epilogue.  setmaxnreg
+// moves registers from the first and third to the epilogue warpgroups, so that an
+// epilogue warp holds its whole 32 x 128 slice of the accumulator at once.
 // Every wait is bounded: past the limit the kernel records a timeout in the
 // device error word, makes the other warps give up, drains its in-flight copies
 // and MMAs, frees TMEM and returns.
@@ -169,12 +174,11 @@ struct Config {
     static constexpr int EPI_COLS = EPI_COLS_;
     static constexpr int EPI_BUFS = EPI_BUFS_;
     // Stream-K needs fp32 accumulation (partials are fp32 sums); the 8-epilogue-warp
-    // configuration has no registers to spare for it and stays data-parallel.
-    static constexpr bool kStreamK =
-        KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4 && !(EPI_BUFS_ == 1 && 2 * EPI_COLS_ == BN_) && !REG_DRAIN_;
+    // (register drain) configuration stays data-parallel.
+    static constexpr bool kStreamK = KIND_ != KIND_F16_ACC16 && EPI_WARPS_ == 4;
     static constexpr int EPI_ROW_BYTES = EPI_COLS * 2;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_ROW_BYTES;
-    // 4 epilogue warps (warps 4-7), or 8 (also warps 13-16): two per TMEM lane
+    // 4 epilogue warps (warps 4-7), or 8 (also warps 12-15): two per TMEM lane
     // quarter, each draining half of the tile's columns.
     static constexpr int EPI_WARPS = EPI_WARPS_;
     static constexpr int EPI_SPLIT = EPI_WARPS / 4;      // column ranges per lane quarter
@@ -185,20 +189,15 @@ struct Config {
     // Staging covers a warp's whole 32-row slice of the tile: the accumulator is
     // drained to shared memory and released before any store is issued.
     static constexpr bool kWholeTileStaging = EPI_COLS * EPI_BUFS == BN / EPI_SPLIT;
-    // Or: one staging buffer, two chunks per warp, no C.  The first chunk is staged,
-    // the second is rounded and held in registers when the accumulator is released,
-    // and staged once the first chunk's store has read the buffer: half the staging
-    // memory of whole-slice staging, with the same early release.  Launched only
-    // without C (the launcher picks a whole-slice instance when C is given).
-    static constexpr bool kHoldLastChunk = !REG_DRAIN_ && EPI_BUFS == 1 && 2 * EPI_COLS == BN / EPI_SPLIT;
     // Register drain (block-scaled pairs, 8 epilogue warps, 512 threads = 4 warpgroups):
     // the issuers / MMA warpgroup and the scale writers give up registers
     // (setmaxnreg) so that each epilogue warp takes its whole 32 x 128 slice of the
     // accumulator into registers with one TMEM round trip and releases it at once;
     // rounding, staging (one 64-column buffer) and stores follow.
     static constexpr bool kRegDrain = REG_DRAIN_;
-    static_assert(!kRegDrain || (EPI_WARPS_ == 8 && EPI_BUFS_ == 1 && 2 * EPI_COLS_ * 2 == BN_),
-                  "register drain: 8 epilogue warps, two 64-column chunks per warp, one staging buffer");
+    static_assert(kRegDrain == (EPI_WARPS_ == 8), "8 epilogue warps exactly in the register-drain layout");
+    static_assert(!kRegDrain || (EPI_BUFS_ == 1 && 2 * EPI_COLS_ * 2 == BN_),
+                  "register drain: two 64-column chunks per warp, one staging buffer");
     // Registers per thread of each warpgroup under kRegDrain (launched with 128):
     // issuers and MMA, epilogue, scale writers, epilogue.  They add up to 4 x 128.
     static constexpr int kRegsIssue = 48, kRegsEpi = 184, kRegsWriter = 96;
@@ -210,9 +209,9 @@ struct Config {
     static constexpr bool kPackedScales = KIND == KIND_NVFP4;
     static_assert(!kRegDrain || kPackedScales, "register drain: NVFP4 (one scale issuer warp)");
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
-    // writers, 12 SFB issuer, 13-16 second epilogue set; with kRegDrain warp 3 issues
-    // both scale streams and warps 12-15 are the second epilogue set.
-    static constexpr int THREADS = kRegDrain ? 512 : (EPI_WARPS == 8 ? 544 : (kBlockScaled ? 416 : 256));
+    // writers, 12 SFB issuer; with kRegDrain warp 3 issues both scale streams and
+    // warps 12-15 are the second epilogue set.
+    static constexpr int THREADS = kRegDrain ? 512 : (kBlockScaled ? 416 : 256);
     // Bytes of K per operand row and stage: 128 (the 128-byte swizzle), or 64 / 32 for
     // problems whose whole K is narrower ("数据布局及其记号", swizzle section: the same
     // hierarchy with 8 x 64-byte and 8 x 32-byte atoms).  32 bytes of K per MMA.
@@ -396,26 +395,6 @@ __device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int
         }
         *slot = pack8<KIND>(f);
     }
-}
-
-// Accumulator words r[0..COLS-1] rounded to COLS / 8 output vectors (no C).
-template <int KIND, int COLS>
-__device__ __forceinline__ void pack_chunk(const uint32_t* r, uint4* out) {
-#pragma unroll
-    for (int v = 0; v < COLS / 8; ++v) {
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
-        out[v] = pack8<KIND>(f);
-    }
-}
-
-// Output vectors of one row into a swizzled staging buffer (the layout stage_chunk writes).
-template <int COLS>
-__device__ __forceinline__ void stage_packed(const uint4* pk, uint8_t* buf, int lane) {
-#pragma unroll
-    for (int v = 0; v < COLS / 8; ++v)
-        *reinterpret_cast<uint4*>(buf + layout::swizzled_offset(COLS * 2, lane, 16 * v)) = pk[v];
 }
 
 // Scale-factor writer for one TMEM lane quarter.  The stage's scale boxes sit in
@@ -838,7 +817,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         constexpr int EC = Cfg::EPI_COLS;
         constexpr int EB = Cfg::EPI_BUFS;
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
-        const int e = warp < 8 ? warp - 4 : (Cfg::kRegDrain ? warp - 8 : warp - 9);  // epilogue warp index
+        const int e = warp < 8 ? warp - 4 : warp - 8;  // epilogue warp index (warps 12-15: 4-7)
         const int c_begin = (e >> 2) * Cfg::BN_EPI;    // this warp's columns of the tile
         const int c_end = c_begin + Cfg::BN_EPI;
         uint8_t* stg = smem + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
@@ -940,9 +919,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (has_c)
                         for (int c = c_begin, b = 0; c < c_end && n0 + c < p.N; c += EC, ++b) load_c(b, n0 + c, m_warp);
                 }
-                __syncwarp();
-            } else if constexpr (Cfg::kHoldLastChunk) {
-                if (rows_in && lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores have read the buffer
                 __syncwarp();
             } else if constexpr (Cfg::kRegDrain) {
                 if (rows_in && lane == 0) {
@@ -1049,56 +1025,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     if (!ok) break;
                 }
-            } else if constexpr (Cfg::kHoldLastChunk) {
-                // Chunk 0 to the staging buffer, chunk 1 rounded into registers; release
-                // the accumulator; store chunk 0, then stage and store chunk 1 (no C).
-                static_assert(!kSK, "whole tiles only");
-                const int c1 = c_begin + EC;
-                const bool have0 = n0 + c_begin < p.N;  // warp-uniform
-                const bool have1 = n0 + c1 < p.N;
-                uint4 pk1[EC / 8];
-                if (have0) {
-                    uint32_t r[EC];
-                    load_chunk<EC>(tacc, c_begin, r);
-                    tmem_ld_wait();
-                    if (rows_in) stage_chunk<KIND, EC, false>(r, stg, lane);
-                }
-                if (have1) {
-#pragma unroll
-                    for (int h = 0; h < EC / 32; ++h) {  // 32 columns at a time: fewer live registers
-                        uint32_t r[32];
-                        load_chunk<32>(tacc, c1 + 32 * h, r);
-                        tmem_ld_wait();
-                        pack_chunk<KIND, 32>(r, pk1 + 4 * h);
-                    }
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (kPair)
-                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
-                    else
-                        mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
-                }
-                if (rows_in && have0) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmD, stg_u32, n0 + c_begin, m_warp);
-                        bulk_commit_group();
-                    }
-                    if (have1) {
-                        if (lane == 0) bulk_wait_group_read<0>();  // chunk 0's store has read the buffer
-                        __syncwarp();
-                        stage_packed<EC>(pk1, stg, lane);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmD, stg_u32, n0 + c1, m_warp);
-                            bulk_commit_group();
-                        }
-                    }
-                }
             } else {
 #pragma unroll 1
                 for (int c = c_begin, b = 0; c < c_end; c += EC, ++b) {
@@ -1182,7 +1108,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mma_role();
     } else if (warp >= 8 && warp < 12) {
         writer_role();
-    } else if ((warp >= 4 && warp < 8) || (Cfg::EPI_WARPS == 8 && warp >= 13 && warp < 17)) {
+    } else if (warp >= 4 && warp < 8) {
         epilogue_role();
     }
 

@@ -10,7 +10,8 @@ context stays usable.
 The test build runs in a child process: two copies of the library (each with
 its own static CUDA runtime) cannot be used in one process.  The FP16 case has two
 single-CTA tiles; the NVFP4 case (two 128 x 128 tiles) also exercises the abandon
-path of the scale issuers and scale writers.
+path of the scale issuers and scale writers; the NVFP4 pair case (two 256 x 256
+tiles, one per CTA pair) that of the pair instance whose warpgroups trade registers.
 """
 import json
 import os
@@ -56,12 +57,13 @@ CHILD = textwrap.dedent(r"""
         t0 = time.time()
         rc = lib.gemm_f16(128, 512, 256, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 0, stream)
     else:
-        prob = inputs.make_problem("nvfp4", 128, 256, 512, seed=32, dist="int", with_c=False)
+        M, N, K, seed = (128, 256, 512, 32) if kind == "nvfp4" else (256, 512, 512, 33)
+        prob = inputs.make_problem("nvfp4", M, N, K, seed=seed, dist="int", with_c=False)
         g = {k: prob[k].to(dev) for k in ("A", "SFA", "B", "SFB")}
-        D = torch.zeros(128, 256, dtype=torch.bfloat16, device=dev)
+        D = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()
         t0 = time.time()
-        rc = lib.gemm_block_scaled(128, 256, 512, g["A"].data_ptr(), g["SFA"].data_ptr(), g["B"].data_ptr(),
+        rc = lib.gemm_block_scaled(M, N, K, g["A"].data_ptr(), g["SFA"].data_ptr(), g["B"].data_ptr(),
                                    g["SFB"].data_ptr(), None, D.data_ptr(), 0, stream)
     status = lib.gemm_last_device_error()
     elapsed = time.time() - t0
@@ -74,8 +76,8 @@ CHILD = textwrap.dedent(r"""
 """)
 
 
-# (kind, output columns computed by CTA 1, which the withheld stage does not affect)
-CASES = [("f16", slice(256, 512)), ("nvfp4", slice(128, 256))]
+# (kind, output columns computed by the second unit, which the withheld stage does not affect)
+CASES = [("f16", slice(256, 512)), ("nvfp4", slice(128, 256)), ("nvfp4pair", slice(256, 512))]
 
 
 @pytest.mark.parametrize("kind,cols", CASES, ids=[c[0] for c in CASES])
@@ -100,8 +102,10 @@ def test_bounded_wait_runs_out_and_is_reported(kind, cols):
     # CTA 1's tile was not affected: exact against the oracle
     if kind == "f16":
         prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
-    else:
+    elif kind == "nvfp4":
         prob = inputs.make_problem("nvfp4", 128, 256, 512, seed=32, dist="int", with_c=False)
+    else:
+        prob = inputs.make_problem("nvfp4", 256, 512, 512, seed=33, dist="int", with_c=False)
     d16, _ = P.oracle_result(prob)
     assert np.array_equal(d_bits[:, cols], d16[:, cols])
     # and this process's product library is unaffected
