@@ -204,9 +204,11 @@ struct Config {
     static_assert(kRegsIssue + kRegsWriter + 2 * kRegsEpi == 4 * 128, "register split adds up to the launch's");
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
-    // NVFP4 stages read their scales from packed 2 KB blocks (one bulk copy per 128
-    // rows); MXFP8, whose 16-byte scale box serves four stages, keeps the TMA boxes.
-    static constexpr bool kPackedScales = KIND == KIND_NVFP4;
+    // NVFP4 stages and MXFP8 CTA-pair stages read their scales from packed 2 KB
+    // blocks (one bulk copy per 128 rows; an MXFP8 block serves four stages).  The
+    // single-CTA MXFP8 instance, whose skinny problems would pay the regrouping pass
+    // on top of a short, memory-bound GEMM, keeps the TMA boxes.
+    static constexpr bool kPackedScales = KIND == KIND_NVFP4 || (KIND == KIND_MXFP8 && PAIR == 2);
     static_assert(!kRegDrain || kPackedScales, "register drain: NVFP4 (one scale issuer warp)");
     // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
     // writers, 12 SFB issuer; with kRegDrain warp 3 issues both scale streams and
@@ -266,7 +268,6 @@ struct Config {
     static_assert(BN % (16 * PAIR) == 0 && BN >= 16 && BN <= 256, "MMA N: multiple of 16 (32 for a pair), <= 256");
     static_assert(B_BYTES % 1024 == 0, "B stages stay 1024-byte aligned");
     static_assert(OFF_EPI % 1024 == 0, "staging buffers start on a swizzle-atom boundary");
-    static_assert(KIND != KIND_MXFP8 || SFB_GROUPS == 1, "MXFP8 scale writer handles one 128-row B group");
 };
 
 // Output tile -> (m block, n block), grouping 8 m blocks so that concurrently
@@ -433,14 +434,15 @@ __device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t
         for (int i = 0; i < (4 * SET) / 16; ++i)
             tmem_st_32x32b_x16(taddr + 16 * i, *reinterpret_cast<const uint32_t(*)[16]>(&out[16 * i]));
     } else {
-        static_assert(SET == 8, "one SFA tile and one SFB tile per stage");
         uint32_t out[SET];
 #pragma unroll
         for (int c = 0; c < SET; ++c) {
             const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * 16 : raw_b + layout::sf_row(lane, c - 4) * 16;
             out[c] = reinterpret_cast<const uint32_t*>(src)[word];
         }
-        tmem_st_32x32b_x8(taddr, out);
+        tmem_st_32x32b_x8(taddr, *reinterpret_cast<const uint32_t(*)[8]>(&out[0]));
+        if constexpr (SET == 12) tmem_st_32x32b_x4(taddr + 8, *reinterpret_cast<const uint32_t(*)[4]>(&out[8]));
+        static_assert(SET == 8 || SET == 12, "one SFA tile and one or two SFB tiles per stage");
     }
 }
 
@@ -608,19 +610,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const int sfx = (KIND == KIND_NVFP4) ? kb * 16 : (kb >> 2) * 16;
                     const uint32_t sb = bar(Cfg::BAR_SFFULL + s);
                     if constexpr (Cfg::kPackedScales) {
-                        // block (row group, 16-byte column kb): the same bytes the box holds
+                        // block (row group, 16-byte column): the same bytes the box holds
                         const size_t cols = static_cast<size_t>(p.sf_cols16);
+                        const int sfc = KIND == KIND_NVFP4 ? kb : (kb >> 2);  // MXFP8: 4 stages per column
                         if (role == 2) {
                             mbar_arrive_expect_tx(sb, Cfg::BM * 16);
                             bulk_load(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
-                                      p.sfa_packed + ((m0 >> 7) * cols + kb) * 2048, 2048, sb);
+                                      p.sfa_packed + ((m0 >> 7) * cols + sfc) * 2048, 2048, sb);
                         }
                         if (role == 3 || Cfg::kRegDrain) {  // kRegDrain: one warp issues both
                             mbar_arrive_expect_tx(sb, Cfg::SFB_GROUPS * 2048);
 #pragma unroll
                             for (int g = 0; g < Cfg::SFB_GROUPS; ++g)
                                 bulk_load(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + g * 2048,
-                                          p.sfb_packed + (((nb0 >> 7) + g) * cols + kb) * 2048, 2048, sb);
+                                          p.sfb_packed + (((nb0 >> 7) + g) * cols + sfc) * 2048, 2048, sb);
                         }
                     } else if (role == 2) {
                         mbar_arrive_expect_tx(sb, Cfg::BM * 16);

@@ -168,26 +168,41 @@ def _one_hot_problem(kind, M, N, K, row, col, sfk):
     return {"kind": kind, "M": M, "N": N, "K": K, "A": A, "B": B, "SFA": SFA, "SFB": SFB, "C": None}
 
 
+# 256 x 264: single-CTA instance; 640 x 3328 (39 tiles of 256 x 256 for 76 SM pairs):
+# CTA-pair instance, whose CTAs each hold all 256 SFB rows of a tile
 @pytest.mark.parametrize("kind", ["nvfp4", "mxfp8"])
 @pytest.mark.parametrize("row,col,sfk", [(0, None, 0), (37, None, 5), (None, 200, 6),
-                                         (127, 129, 15), (64, None, 2), (None, 31, 3)])
-def test_one_hot_scale_probe(kind, row, col, sfk):
+                                         (127, 129, 15), (64, None, 2), (None, 31, 3), (300, 2900, 9)])
+@pytest.mark.parametrize("M,N,K", [(256, 264, 1024), (640, 3328, 512)])
+def test_one_hot_scale_probe(kind, row, col, sfk, M, N, K):
     """All data 1 and all scales 1 except one SFA row or SFB column block set to 2:
     only that row / column of D moves, by K_blk."""
-    prob = _one_hot_problem(kind, 256, 264, 1024, row, col, sfk)
+    if row is not None and row >= M or col is not None and col >= N:
+        pytest.skip("probe outside this shape")
+    prob = _one_hot_problem(kind, M, N, K, row, col, sfk)
     D = P.run_gpu(prob)
     P.check(prob, D, mode="exact")
+
+
+@pytest.mark.parametrize("kind", ["nvfp4", "mxfp8"])
+@pytest.mark.parametrize("with_c", [False, True])
+def test_block_scaled_pair_integers_bit_exact(kind, with_c):
+    # 1000 x 2504: 40 tiles of 256 x 256 (CTA-pair instance), ragged in M and N
+    prob = inputs.make_problem(kind, 1000, 2504, 512, seed=15, dist="int", with_c=with_c)
+    P.check(prob, P.run_gpu(prob), mode="exact")
 
 
 # ------------------------------------------------------------------ MXFP8
 
 @pytest.mark.parametrize("with_c", [False, True])
-def test_mxfp8_integers_bit_exact(with_c):
-    prob = inputs.make_problem("mxfp8", 128, 256, 1024, seed=14, dist="int", with_c=with_c)
+@pytest.mark.parametrize("M", [128, 384])
+def test_mxfp8_integers_bit_exact(with_c, M):
+    # M = 384: CTA-pair instance (256-row tiles, the second one ragged), packed scales
+    prob = inputs.make_problem("mxfp8", M, 256, 1024, seed=14, dist="int", with_c=with_c)
     P.check(prob, P.run_gpu(prob), mode="exact")
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 392, 1024), (128, 136, 512), (64, 2048, 4096)])
+@pytest.mark.parametrize("M,N,K", [(300, 392, 1024), (128, 136, 512), (64, 2048, 4096), (2048, 4096, 2048)])
 def test_mxfp8_random_tolerance(M, N, K):
     prob = inputs.make_problem("mxfp8", M, N, K, seed=M + N, dist="normal", with_c=True)
     P.check(prob, P.run_gpu(prob), mode="tol")
