@@ -65,6 +65,7 @@ WORKLOADS = {
         Workload("mxfp8_128x16384", KIND_MXFP8, 128, 16384, 8192, "normal", True, 0, 4),
         Workload("bf16_4096", KIND_BF16, 4096, 4096, 4096, "normal0.1", True, 0, 5),
         Workload("fp8e4m3_8192", KIND_FP8_E4M3, 8192, 8192, 8192, "normal", False, 0, 6),
+        Workload("mxfp8_8192", KIND_MXFP8, 8192, 8192, 8192, "normal", False, 0, 7),
     ]
 }
 

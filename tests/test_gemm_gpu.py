@@ -208,6 +208,15 @@ def test_mxfp8_random_tolerance(M, N, K):
     P.check(prob, P.run_gpu(prob), mode="tol")
 
 
+def test_mxfp8_8192_full_size_sampled_rows():
+    # MXFP8 at the NVFP4 workload's size: CTA-pair instance, 32 x 32 tiles over 76 SM pairs
+    prob = inputs.workload_problem("mxfp8_8192")
+    D = P.run_gpu(prob)
+    rows = P.sample_rows(prob["M"], 16, seed=4)
+    P.check(prob, D, rows=rows, mode="tol")
+    assert torch.isfinite(D.float()).all()
+
+
 def test_nvfp4_8192_full_size_sampled_rows():
     prob = inputs.workload_problem("nvfp4_8192")
     D = P.run_gpu(prob)
