@@ -88,9 +88,10 @@ def test_fp8e4m3_8192_full_size_sampled_rows():
 
 # ------------------------------------------------------------------ in place, guard bands, concurrency
 
-@pytest.mark.parametrize("kind", ["nvfp4", "mxfp8", "fp8e4m3"])
-def test_in_place_d_is_c(kind):
-    M, N, K = (300, 264, 1024) if kind != "mxfp8" else (200, 256, 1024)
+@pytest.mark.parametrize("kind,M,N,K", [("nvfp4", 300, 264, 1024), ("mxfp8", 200, 256, 1024), ("fp8e4m3", 300, 264, 1024),
+                                        ("nvfp4", 1000, 2504, 512), ("mxfp8", 1000, 2504, 512)])
+def test_in_place_d_is_c(kind, M, N, K):
+    # 1000 x 2504: 40 tiles of 256 x 256, the block-scaled CTA-pair instance
     prob = inputs.make_problem(kind, M, N, K, seed=61, dist="int", with_c=True)
     g = P.to_device(prob, P.device())
     D = g["C"].clone()
@@ -103,7 +104,8 @@ def test_in_place_d_is_c(kind):
     P.check(prob, D.cpu(), mode="exact")
 
 
-@pytest.mark.parametrize("kind,M,N,K", [("nvfp4", 130, 264, 512), ("fp8e5m2", 129, 136, 1008), ("bf16", 257, 8, 72)])
+@pytest.mark.parametrize("kind,M,N,K", [("nvfp4", 130, 264, 512), ("fp8e5m2", 129, 136, 1008), ("bf16", 257, 8, 72),
+                                        ("mxfp8", 1000, 2504, 512)])
 def test_guard_bands_untouched(kind, M, N, K):
     # D sits between NaN guard bands; ragged M and N must not write outside it
     prob = inputs.make_problem(kind, M, N, K, seed=62, dist="int" if kind != "bf16" else "int2", with_c=True)
