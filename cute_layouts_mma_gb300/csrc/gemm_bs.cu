@@ -39,18 +39,21 @@ std::atomic<uintptr_t> g_err_addr[kMaxDevices];
 unsigned int* err_word(int dev) { return device_symbol(g_err_bs, g_err_addr, dev); }
 
 // One scale matrix to regroup: src [rows][cols16 * 16] bytes, row-major; dst
-// [groups][cols16][128][16], rows at or past `rows` zero.
+// [groups][cols16][group_rows][16] (group_rows a multiple of 32), rows at or past
+// `rows` zero.
 struct PackJob {
     const uint8_t* src;
     uint8_t* dst;
     int rows;
     int groups;
+    int group_rows;
 };
 
-// Regroups SFA and SFB into the packed blocks the NVFP4 stages load (one warp per
-// 2 KB block: lane l moves rows l, l+32, l+64, l+96 of the block, so each store
-// instruction writes 512 contiguous bytes).  A block holds exactly the bytes of the
-// 16-byte x 128-row scale box of one stage, in the same row-major order.
+// Regroups SFA (128-row groups: one CTA's rows) and SFB (one group per tile's
+// columns) into the packed blocks the stages load, one warp per block: lane l
+// moves rows l, l+32, ... of the block, so each store instruction writes 512
+// contiguous bytes.  A block holds exactly the bytes of the 16-byte-wide scale box
+// of one stage, in the same row-major order.
 __global__ void __launch_bounds__(256) pack_scales_kernel(PackJob a, PackJob b, int cols16) {
     griddep_wait();  // the scales may be written by the previous launch on the stream
     griddep_launch_dependents();
@@ -62,23 +65,22 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(PackJob a, PackJob b, 
     const int blk = w < blocks_a ? w : w - blocks_a;
     const int g = blk / cols16, c = blk - g * cols16;
     const size_t pitch = static_cast<size_t>(cols16) * 16;
-    uint4* out = reinterpret_cast<uint4*>(j.dst + static_cast<size_t>(blk) * 2048);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = 32 * i + lane;
-        const int row = g * 128 + r;
+    uint4* out = reinterpret_cast<uint4*>(j.dst + static_cast<size_t>(blk) * j.group_rows * 16);
+    for (int r = lane; r < j.group_rows; r += 32) {
+        const int row = g * j.group_rows + r;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (row < j.rows) v = __ldg(reinterpret_cast<const uint4*>(j.src + static_cast<size_t>(row) * pitch + 16 * c));
         out[r] = v;
     }
 }
 
-// Enqueue the regrouping of SFA (ga row groups) and SFB (gb) into `packed` on `stream`.
-cudaError_t launch_pack(const void* SFA, int64_t M, int ga, const void* SFB, int64_t N, int gb, int cols16,
-                        uint8_t* packed, cudaStream_t stream) {
-    const PackJob a{static_cast<const uint8_t*>(SFA), packed, static_cast<int>(M), ga};
-    const PackJob b{static_cast<const uint8_t*>(SFB), packed + static_cast<size_t>(ga) * cols16 * 2048,
-                    static_cast<int>(N), gb};
+// Enqueue the regrouping of SFA (ga groups of 128 rows) and SFB (gb groups of gb_rows)
+// into `packed` on `stream`: SFA's blocks first, then SFB's.
+cudaError_t launch_pack(const void* SFA, int64_t M, int ga, const void* SFB, int64_t N, int gb, int gb_rows,
+                        int cols16, uint8_t* packed, cudaStream_t stream) {
+    const PackJob a{static_cast<const uint8_t*>(SFA), packed, static_cast<int>(M), ga, 128};
+    const PackJob b{static_cast<const uint8_t*>(SFB), packed + static_cast<size_t>(ga) * cols16 * 128 * 16,
+                    static_cast<int>(N), gb, gb_rows};
     const long long warps = static_cast<long long>(ga + gb) * cols16;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
@@ -135,17 +137,20 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
     if constexpr (Cfg::kPackedScales) {
         // Packed scales for this call, taken from the device's stream-ordered pool and
         // returned on the same stream after the GEMM.  Row groups cover whole tiles.
+        // SFA in groups of 128 rows (one CTA's rows), SFB in groups of BN rows (one tile).
         const int cols16 = static_cast<int>(sf_cols / 16);
         const int ga = p.num_m_blocks * (Cfg::BM_TILE / 128);
-        const int gb = p.num_n_blocks * Cfg::SFB_GROUPS;
+        const int gb = p.num_n_blocks;
+        const size_t a_bytes = static_cast<size_t>(ga) * cols16 * 128 * 16;
+        const size_t b_bytes = static_cast<size_t>(gb) * cols16 * Cfg::BN * 16;
         void* packed = nullptr;
-        if (cudaMallocFromPoolAsync(&packed, (static_cast<size_t>(ga) + gb) * cols16 * 2048, scratch_pool(dev),
-                                    stream) != cudaSuccess)
+        if (cudaMallocFromPoolAsync(&packed, a_bytes + b_bytes, scratch_pool(dev), stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
         p.sfa_packed = static_cast<const uint8_t*>(packed);
-        p.sfb_packed = static_cast<const uint8_t*>(packed) + static_cast<size_t>(ga) * cols16 * 2048;
+        p.sfb_packed = static_cast<const uint8_t*>(packed) + a_bytes;
         p.sf_cols16 = cols16;
-        cudaError_t e = launch_pack(SFA, M, ga, SFB, N, gb, cols16, static_cast<uint8_t*>(packed), stream);
+        cudaError_t e =
+            launch_pack(SFA, M, ga, SFB, N, gb, Cfg::BN, cols16, static_cast<uint8_t*>(packed), stream);
         if (e == cudaSuccess) e = launch_config<Cfg>(ta, tb, tsa, tsb, td, tc, p, sms, dev, stream);
         const cudaError_t f = cudaFreeAsync(packed, stream);
         if (e != cudaSuccess || f != cudaSuccess) return GEMM_ERR_CUDA;

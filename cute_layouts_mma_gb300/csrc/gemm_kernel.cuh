@@ -107,9 +107,10 @@ struct Params {
     float* ws;             // partials: [unit][rank][epilogue warp][chunk][col/4][lane][4]
     unsigned int* flags;   // [unit][rank][epilogue warp]: 1 once that partial is written
     // Block-scaled kinds with packed scales (Config::kPackedScales): SFA and SFB
-    // regrouped into contiguous 2 KB blocks [row group of 128][16-byte scale column]
-    // [128 rows][16 bytes] (rows past the matrix are zero), so that one stage's
-    // scales of 128 rows arrive in one bulk copy instead of 128 strided 16-byte rows.
+    // regrouped into contiguous blocks [row group][16-byte scale column][rows][16 bytes]
+    // (SFA: groups of 128 rows; SFB: groups of BN rows, one per tile; rows past the
+    // matrix are zero), so that one stage's scales of a row group arrive in one bulk
+    // copy instead of one strided 16-byte row at a time.
     const uint8_t* sfa_packed;
     const uint8_t* sfb_packed;
     int sf_cols16;  // 16-byte scale columns per row (blocks per row group)
@@ -227,6 +228,8 @@ struct Config {
     static constexpr int A_BYTES = BM * kRowBytes;
     static constexpr int B_BYTES = BN_CTA * kRowBytes;
     static constexpr int SFB_GROUPS = kBlockScaled ? (BN + 127) / 128 : 0;  // 128-row scale groups
+    static constexpr int SFB_TCOLS = kBlockScaled ? BN / 32 : 0;             // TMEM columns of a tile's SFB
+    static_assert(!kBlockScaled || BN % 32 == 0, "block-scaled tiles of whole 32-row scale columns");
     static constexpr int SFA_BYTES = kBlockScaled ? BM * 16 : 0;
     static constexpr int SFB_BYTES = SFB_GROUPS * 128 * 16;
     static constexpr uint32_t TX_BYTES = PAIR * (A_BYTES + B_BYTES);             // both CTAs' operands
@@ -253,7 +256,7 @@ struct Config {
 
     // TMEM (per CTA): ACC_BUFS accumulators of BN fp32 columns, then the scale slots.
     static constexpr int SF_COL0 = ACC_BUFS * BN;
-    static constexpr int SF_COLS_PER_COPYSET = 4 * (1 + SFB_GROUPS);  // SFA tile + SFB tiles (one MMA)
+    static constexpr int SF_COLS_PER_COPYSET = 4 + SFB_TCOLS;  // SFA tile (TCol = m // 32) + SFB (n // 32)
     static constexpr int SF_COLS_PER_STAGE =
         KIND == KIND_NVFP4 ? kMmasPerStage * SF_COLS_PER_COPYSET
                            : (KIND == KIND_MXFP8 ? SF_COLS_PER_COPYSET : 0);
@@ -409,10 +412,10 @@ __device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int
 // per stage (word `word` of each row = the stage's 4 scales, one per MMA, picked
 // by the MMA's scale-factor ID).  Every quarter writes the same values: together
 // the four warps replicate the tile to the four lane partitions.
-template <int KIND, int GROUPS>
+template <int KIND, int SFB_TCOLS>
 __device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t* raw_b, int lane, int word,
                                              uint32_t taddr) {
-    constexpr int SET = 4 + 4 * GROUPS;
+    constexpr int SET = 4 + SFB_TCOLS;  // SFA columns (128 rows) + SFB columns (BN rows)
     if constexpr (KIND == KIND_NVFP4) {
         uint32_t R[SET][4];
 #pragma unroll
@@ -619,11 +622,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                       p.sfa_packed + ((m0 >> 7) * cols + sfc) * 2048, 2048, sb);
                         }
                         if (role == 3 || Cfg::kRegDrain) {  // kRegDrain: one warp issues both
-                            mbar_arrive_expect_tx(sb, Cfg::SFB_GROUPS * 2048);
-#pragma unroll
-                            for (int g = 0; g < Cfg::SFB_GROUPS; ++g)
-                                bulk_load(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + g * 2048,
-                                          p.sfb_packed + (((nb0 >> 7) + g) * cols + sfc) * 2048, 2048, sb);
+                            // SFB blocks hold a whole tile's BN rows
+                            constexpr uint32_t kSfbBlock = BN * 16;
+                            mbar_arrive_expect_tx(sb, kSfbBlock);
+                            bulk_load(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES,
+                                      p.sfb_packed + (static_cast<size_t>(nb) * cols + sfc) * kSfbBlock, kSfbBlock, sb);
                         }
                     } else if (role == 2) {
                         mbar_arrive_expect_tx(sb, Cfg::BM * 16);
@@ -759,6 +762,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         s = 0;
                         ph ^= 1u;
                     }
+
                 }
                 (void)tile;
                 (void)kind;
@@ -793,7 +797,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 for (int kb = k0; kb < k1; ++kb) {
                     ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_SFFULL + s), ph, abort_flag, p.err));
                     if (!ok) break;
-                    write_scales<KIND, Cfg::SFB_GROUPS>(
+                    write_scales<KIND, Cfg::SFB_TCOLS>(
                         smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, lane,
                         kb & 3, lane_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE));
                     tmem_st_wait();
@@ -811,6 +815,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         s = 0;
                         ph ^= 1u;
                     }
+
                 }
             }
         }
