@@ -17,6 +17,9 @@ using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
 // pieces.  The pair instance fits 8 stages of 24 KiB.
 using CfgF16N128Pair = Config<KIND_F16_ACC32, 128, 8, 2, 64, 2, 2>;
 using CfgF16N128 = Config<KIND_F16_ACC32, 128, 6, 2, 64, 2, 1>;
+// Small problems (use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages, each
+// epilogue warp staging its whole 32 x 64 slice.
+using CfgF16N64 = Config<KIND_F16_ACC32, 64, 4, 2, 64, 1, 1>;
 // Narrow K (fp32 accumulation): a whole K of at most 32 or 16 elements fits a 64- or
 // 32-byte operand row, stored with the 64- or 32-byte swizzle; 2 or 1 MMAs per stage
 // instead of 4 over zero-filled K.  These launches are bound by the C and D traffic,
@@ -91,6 +94,8 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
         if (K <= 32)
             return pair ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                         : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
+        if (pair ? use_small_tiles<CfgF16Acc32Pair>(M, N, K, 64, sms) : use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms))
+            return run<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
         if (pair)
             return would_split<CfgF16Acc32Pair>(M, N, K, 64, sms) ? run<CfgF16N128Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                                                                    : run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
@@ -146,6 +151,8 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const 
 gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                                       void* D, cudaStream_t stream, int sms, int dev) {
     // the same instance choice as gemm_f16 with fp32 accumulation and K > 32
+    if (M > 128 ? use_small_tiles<CfgF16Acc32Pair>(M, N, K, 64, sms) : use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms))
+        return run_noalloc<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
     if (M > 128)
         return would_split<CfgF16Acc32Pair>(M, N, K, 64, sms)
                    ? run_noalloc<CfgF16N128Pair>(M, N, K, A, B, C, D, stream, sms, dev)

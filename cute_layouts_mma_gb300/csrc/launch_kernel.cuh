@@ -102,6 +102,21 @@ bool would_split(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
     return choose_schedule<Cfg>(q, Cfg::PAIR == 2 ? sms / 2 : sms).sk_tiles != 0;
 }
 
+// Small problems: whole tiles of `Big` (256 columns; CTA pairs for M > 128) would keep
+// fewer than half of the units busy, K is short (at most 1024) and no stream-K split
+// applies.  Such a launch is bound by each CTA's operand loads and its fixed latency,
+// so the launchers switch to 128 x 64 tiles on single CTAs: many more CTAs, each
+// loading a fraction of the bytes (FP16 256^3: 5.3 -> 3.7 us per call on GB300).
+// Long K keeps the big tiles: an N = 64 MMA is too short for the single issuing
+// thread to keep the tensor pipe busy.
+template <class Big>
+bool use_small_tiles(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
+    if (K > 1024) return false;
+    const int64_t tiles = ((M + Big::BM_TILE - 1) / Big::BM_TILE) * ((N + Big::BN - 1) / Big::BN);
+    const int units = Big::PAIR == 2 ? sms / 2 : sms;
+    return 2 * tiles < units && !would_split<Big>(M, N, K, k_per_block, sms);
+}
+
 template <class Cfg>
 cudaError_t prepare_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int sms, int dev,
                            cudaStream_t stream, int* units_out) {

@@ -146,3 +146,17 @@ def test_gemm_dtype_dispatch(dtype):
     D = tg.gemm(A, B, g["C"])
     torch.cuda.synchronize()
     P.check(prob, D.cpu(), mode="exact")
+
+
+# ------------------------------------------------------------------ instance choice by size
+
+# Short-K problems whose 256-column tiles would keep fewer than half of the units busy take
+# 128 x 64 tiles (most of the small shapes above); these sizes keep the 256-column tiles:
+# 1000 x 2504 (40 CTA-pair tiles) and 120 x 19600 (77 single-CTA tiles), ragged edges.
+@pytest.mark.parametrize("kind", ["f16", "bf16", "fp8e4m3"])
+@pytest.mark.parametrize("M,N,K", [(1000, 2504, 512), (120, 19600, 256)])
+def test_big_tile_sizes_bit_exact(kind, M, N, K):
+    prob = inputs.make_problem(kind, M, N, K, seed=M + N + K, dist="int" if kind == "fp8e4m3" else "int2",
+                               with_c=True)
+    D = P.run_gpu(prob, accum=0) if kind == "f16" else P.run_gpu(prob)
+    P.check(prob, D, mode="exact")
