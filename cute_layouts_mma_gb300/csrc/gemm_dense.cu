@@ -16,11 +16,8 @@ using CfgE4m3 = Config<KIND_FP8_E4M3, 256, 4, 2, 64, 2, 1>;
 using CfgE5m2Pair = Config<KIND_FP8_E5M2, 256, 6, 2, 64, 2, 2>;
 using CfgE5m2 = Config<KIND_FP8_E5M2, 256, 4, 2, 64, 2, 1>;
 // Skinny problems that the 256-column instances would split: 128-column tiles (as FP16).
-using CfgBf16N128Pair = Config<KIND_BF16, 128, 8, 2, 64, 2, 2>;
 using CfgBf16N128 = Config<KIND_BF16, 128, 6, 2, 64, 2, 1>;
-using CfgE4m3N128Pair = Config<KIND_FP8_E4M3, 128, 8, 2, 64, 2, 2>;
 using CfgE4m3N128 = Config<KIND_FP8_E4M3, 128, 6, 2, 64, 2, 1>;
-using CfgE5m2N128Pair = Config<KIND_FP8_E5M2, 128, 8, 2, 64, 2, 2>;
 using CfgE5m2N128 = Config<KIND_FP8_E5M2, 128, 6, 2, 64, 2, 1>;
 // Small problems (use_small_tiles): 128 x 64 tiles on single CTAs.
 using CfgBf16N64 = Config<KIND_BF16, 64, 4, 2, 64, 1, 1>;
@@ -75,18 +72,15 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
 
 namespace {
 
-// CTA pairs for M > 128, single CTAs otherwise; the 128-column instance where the
-// 256-column one would split tiles across units; 128 x 64 tiles for small problems.
-template <class Pair, class Single, class PairN128, class SingleN128, class SmallN64>
+// CTA pairs when their tiles fill every SM pair (use_pairs); otherwise single CTAs:
+// 128 x 64 tiles for small problems, the 128-column instance where the 256-column one
+// would split tiles across units.
+template <class Pair, class Single, class SingleN128, class SmallN64>
 gemm_status_t dispatch(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
                        cudaStream_t stream, int sms, int dev) {
-    if (M > 128 ? use_small_tiles<Pair>(M, N, K, Pair::kKCoordPerStage, sms)
-                : use_small_tiles<Single>(M, N, K, Single::kKCoordPerStage, sms))
+    if (use_pairs(M, N, sms)) return run<Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+    if (use_small_tiles<Single>(M, N, K, Single::kKCoordPerStage, sms))
         return run<SmallN64>(M, N, K, A, B, C, D, stream, sms, dev);
-    if (M > 128)
-        return would_split<Pair>(M, N, K, Pair::kKCoordPerStage, sms)
-                   ? run<PairN128>(M, N, K, A, B, C, D, stream, sms, dev)
-                   : run<Pair>(M, N, K, A, B, C, D, stream, sms, dev);
     return would_split<Single>(M, N, K, Single::kKCoordPerStage, sms)
                ? run<SingleN128>(M, N, K, A, B, C, D, stream, sms, dev)
                : run<Single>(M, N, K, A, B, C, D, stream, sms, dev);
@@ -96,14 +90,14 @@ gemm_status_t dispatch(int64_t M, int64_t N, int64_t K, const void* A, const voi
 
 gemm_status_t launch_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                                void* D, cudaStream_t stream, int sms, int dev) {
-    return dispatch<CfgBf16Pair, CfgBf16, CfgBf16N128Pair, CfgBf16N128, CfgBf16N64>(M, N, K, A, B, C, D, stream, sms, dev);
+    return dispatch<CfgBf16Pair, CfgBf16, CfgBf16N128, CfgBf16N64>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
 gemm_status_t launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                               void* D, int fmt, cudaStream_t stream, int sms, int dev) {
     if (fmt == GEMM_FP8_E4M3)
-        return dispatch<CfgE4m3Pair, CfgE4m3, CfgE4m3N128Pair, CfgE4m3N128, CfgE4m3N64>(M, N, K, A, B, C, D, stream, sms, dev);
-    return dispatch<CfgE5m2Pair, CfgE5m2, CfgE5m2N128Pair, CfgE5m2N128, CfgE5m2N64>(M, N, K, A, B, C, D, stream, sms, dev);
+        return dispatch<CfgE4m3Pair, CfgE4m3, CfgE4m3N128, CfgE4m3N64>(M, N, K, A, B, C, D, stream, sms, dev);
+    return dispatch<CfgE5m2Pair, CfgE5m2, CfgE5m2N128, CfgE5m2N64>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
 unsigned int read_clear_error_dense() { return read_clear_word(g_err_dense); }

@@ -5,17 +5,16 @@
 
 namespace tn {
 
-// CTA pairs (M > 128): 256 x 256 tiles, 6 stages of 64 K, two TMEM accumulators,
+// CTA pairs (use_pairs): 256 x 256 tiles, 6 stages of 64 K, two TMEM accumulators,
 // epilogue staged in 32 x 64 chunks (128-byte rows), double-buffered.
 using CfgF16Acc32Pair = Config<KIND_F16_ACC32, 256, 6, 2, 64, 2, 2>;
 using CfgF16Acc16Pair = Config<KIND_F16_ACC16, 256, 6, 2, 64, 2, 2>;
-// Single CTAs (M <= 128): 128 x 256 tiles, 4 stages.
+// Single CTAs: 128 x 256 tiles, 4 stages.
 using CfgF16Acc32 = Config<KIND_F16_ACC32, 256, 4, 2, 64, 2, 1>;
 using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
 // Skinny problems whose 256-column tiles would leave most units idle (fp32
 // accumulation): 128-column tiles, so stream-K cuts each tile into fewer, smaller
-// pieces.  The pair instance fits 8 stages of 24 KiB.
-using CfgF16N128Pair = Config<KIND_F16_ACC32, 128, 8, 2, 64, 2, 2>;
+// pieces.
 using CfgF16N128 = Config<KIND_F16_ACC32, 128, 6, 2, 64, 2, 1>;
 // Small problems (use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages, each
 // epilogue warp staging its whole 32 x 64 slice.
@@ -86,19 +85,17 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
 
 gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                               void* D, int accum, cudaStream_t stream, int sms, int dev) {
-    const bool pair = M > 128;
+    const bool pair = use_pairs(M, N, sms);
     if (accum == GEMM_ACC_F32) {
+        // narrow K: bound by the C and D traffic, pairs whenever M > 128
         if (K <= 16)
-            return pair ? run<CfgF16K16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
-                        : run<CfgF16K16>(M, N, K, A, B, C, D, stream, sms, dev);
+            return M > 128 ? run<CfgF16K16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                           : run<CfgF16K16>(M, N, K, A, B, C, D, stream, sms, dev);
         if (K <= 32)
-            return pair ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
-                        : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
-        if (pair ? use_small_tiles<CfgF16Acc32Pair>(M, N, K, 64, sms) : use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms))
-            return run<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
-        if (pair)
-            return would_split<CfgF16Acc32Pair>(M, N, K, 64, sms) ? run<CfgF16N128Pair>(M, N, K, A, B, C, D, stream, sms, dev)
-                                                                   : run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+            return M > 128 ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                           : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
+        if (pair) return run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+        if (use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms)) return run<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
         return would_split<CfgF16Acc32>(M, N, K, 64, sms) ? run<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev)
                                                            : run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
     }
@@ -151,12 +148,9 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const 
 gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                                       void* D, cudaStream_t stream, int sms, int dev) {
     // the same instance choice as gemm_f16 with fp32 accumulation and K > 32
-    if (M > 128 ? use_small_tiles<CfgF16Acc32Pair>(M, N, K, 64, sms) : use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms))
+    if (use_pairs(M, N, sms)) return run_noalloc<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+    if (use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms))
         return run_noalloc<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
-    if (M > 128)
-        return would_split<CfgF16Acc32Pair>(M, N, K, 64, sms)
-                   ? run_noalloc<CfgF16N128Pair>(M, N, K, A, B, C, D, stream, sms, dev)
-                   : run_noalloc<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
     return would_split<CfgF16Acc32>(M, N, K, 64, sms) ? run_noalloc<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev)
                                                        : run_noalloc<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
 }

@@ -102,6 +102,15 @@ bool would_split(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
     return choose_schedule<Cfg>(q, Cfg::PAIR == 2 ? sms / 2 : sms).sk_tiles != 0;
 }
 
+// Dense kinds: CTA pairs (256 x 256 tiles) once their tiles fill every SM pair at least
+// once; below that the single-CTA instances (128 x 256, or 128 x 128 with stream-K, or
+// 128 x 64) spread the work over twice as many units.  Measured on GB300 (FP16, no C):
+// 512 x 8192 x 2048 14.5 -> 13.7 us, 2048^2 x 1024 10.0 -> 9.1, 256 x 2048 x 8192
+// 26.5 -> 22.7; 4096^2 x 1024 (256 pair tiles) stays on pairs (24.0 against 26.5).
+inline bool use_pairs(int64_t M, int64_t N, int sms) {
+    return M > 128 && ((M + 255) / 256) * ((N + 255) / 256) >= sms / 2;
+}
+
 // Small problems: whole tiles of `Big` (256 columns; CTA pairs for M > 128) would keep
 // fewer than half of the units busy, K is short (at most 1024) and no stream-K split
 // applies.  Such a launch is bound by each CTA's operand loads and its fixed latency,
