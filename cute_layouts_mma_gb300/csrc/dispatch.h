@@ -1,0 +1,108 @@
+// Instance choice of the launchers: which tile shape and schedule a problem gets.
+// Host-only and free of CUDA types, so that the CPU tests can hold the rules
+// against the table of measured choices without a GPU.  The launchers
+// (gemm_f16.cu, gemm_dense.cu, gemm_bs.cu, launch_kernel.cuh) call these with the
+// constants of their kernel instances.
+#pragma once
+
+#include <cstdint>
+
+namespace tn {
+namespace dispatch {
+
+// Stream-K is used when whole tiles would leave more than three quarters of the
+// units idle, each unit's share is at least kStreamKMinShare k-blocks, and the
+// accumulation is fp32.  Outside that range, measurement on GB300 favoured whole
+// tiles: once a quarter of the SMs stream operands, skinny problems are bound by
+// HBM rather than by SM count; dense FP16 runs at the power limit, where idle SMs
+// raise the clock of the busy ones; and short shares leave each split tile in many
+// pieces whose partials the finishing unit adds one after another.
+constexpr double kStreamKMinIdle = 0.75;
+constexpr long long kStreamKMinShare = 12;
+
+// The shape of an instance's output tiles, as far as the schedule is concerned.
+struct TileShape {
+    int bm_tile;    // output rows per tile (128, or 256 for a CTA pair)
+    int bn;         // output columns per tile
+    int pair;       // CTAs per tile (1 or 2)
+    bool stream_k;  // the instance can split tiles (fp32 partials)
+};
+
+// Schedule of one launch: units used and how many tiles (the last ones) are split.
+struct Schedule {
+    int units;
+    int sk_tiles;
+};
+
+inline Schedule choose_schedule(long long tiles, int num_k_blocks, int max_units, bool stream_k) {
+    Schedule sc{static_cast<int>(tiles < max_units ? tiles : max_units), 0};
+    if (!stream_k || tiles <= 0) return sc;
+    const long long rounds = (tiles + max_units - 1) / max_units;
+    const double idle = 1.0 - static_cast<double>(tiles) / static_cast<double>(rounds * max_units);
+    if (idle <= kStreamKMinIdle) return sc;
+    const long long split = tiles % max_units;  // the tiles of the last, partly idle round
+    if (split * num_k_blocks < kStreamKMinShare * max_units) return sc;
+    return Schedule{max_units, static_cast<int>(split)};
+}
+
+inline long long tile_count(int64_t M, int64_t N, const TileShape& t) {
+    return ((M + t.bm_tile - 1) / t.bm_tile) * ((N + t.bn - 1) / t.bn);
+}
+
+inline int units_of(const TileShape& t, int sms) { return t.pair == 2 ? sms / 2 : sms; }
+
+// Whether an instance's own schedule would split tiles for this problem (units
+// estimated as one per SM, or one per SM pair).
+inline bool would_split(int64_t M, int64_t N, int64_t K, int k_per_block, int sms, const TileShape& t) {
+    const int nkb = static_cast<int>((K + k_per_block - 1) / k_per_block);
+    return choose_schedule(tile_count(M, N, t), nkb, units_of(t, sms), t.stream_k).sk_tiles != 0;
+}
+
+// Dense kinds: CTA pairs (256 x 256 tiles) once their tiles fill every SM pair at least
+// once; below that the single-CTA instances (128 x 256, or 128 x 128 with stream-K, or
+// 128 x 64) spread the work over twice as many units.  Measured on GB300 (FP16, no C):
+// 512 x 8192 x 2048 14.5 -> 13.9 us, 2048^2 x 1024 10.0 -> 9.2, 256 x 2048 x 8192
+// 26.5 -> 22.8; 4096^2 x 1024 (256 pair tiles) stays on pairs.
+inline bool use_pairs(int64_t M, int64_t N, int sms) {
+    return M > 128 && ((M + 255) / 256) * ((N + 255) / 256) >= sms / 2;
+}
+
+// Small problems: whole tiles of `big` would keep fewer than half of the units busy,
+// K is short (at most 1024) and no stream-K split applies.  Such a launch is bound by
+// each CTA's operand loads and its fixed latency, so the launchers switch to 128 x 64
+// tiles on single CTAs: many more CTAs, each loading a fraction of the bytes (FP16
+// 256^3: 5.3 -> 3.7 us per call on GB300).  Long K keeps the big tiles: an N = 64 MMA
+// is too short for the single issuing thread to keep the tensor pipe busy.
+inline bool use_small_tiles(int64_t M, int64_t N, int64_t K, int k_per_block, int sms, const TileShape& big) {
+    if (K > 1024) return false;
+    return 2 * tile_count(M, N, big) < units_of(big, sms) && !would_split(M, N, K, k_per_block, sms, big);
+}
+
+// Tile shapes of the dense instances (FP16 with fp32 accumulation, BF16, FP8), K > 32.
+constexpr TileShape kDensePair256{256, 256, 2, true};
+constexpr TileShape kDenseSingle256{128, 256, 1, true};
+constexpr TileShape kDenseSingle128{128, 128, 1, true};
+constexpr TileShape kDenseSingle64{128, 64, 1, true};
+
+enum DenseChoice { DENSE_PAIR_256 = 0, DENSE_SINGLE_256 = 1, DENSE_SINGLE_128 = 2, DENSE_SINGLE_64 = 3 };
+
+// CTA pairs when their tiles fill every SM pair; otherwise single CTAs: 128 x 64 tiles
+// for small problems, the 128-column instance where the 256-column one would split.
+inline DenseChoice dense_choice(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
+    if (use_pairs(M, N, sms)) return DENSE_PAIR_256;
+    if (use_small_tiles(M, N, K, k_per_block, sms, kDenseSingle256)) return DENSE_SINGLE_64;
+    return would_split(M, N, K, k_per_block, sms, kDenseSingle256) ? DENSE_SINGLE_128 : DENSE_SINGLE_256;
+}
+
+// Block-scaled kinds: CTA pairs (256 x 256 tiles, whole tiles only) when M > 128 and the
+// pair tiles fill at least half of the device's SM pairs; otherwise the single-CTA
+// 128 x 128 instances, which also split skinny problems with stream-K.  Measured on
+// GB300 (NVFP4 and MXFP8, K = 8192-16384): pairs faster from 40 tiles (1024 x 2560) up,
+// single CTAs faster at 32 tiles (512 x 4096) and 16 tiles (256 x 4096).
+inline bool use_block_scaled_pair(int64_t M, int64_t N, int sms) {
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    return M > 128 && 2 * pair_tiles >= sms / 2;
+}
+
+}  // namespace dispatch
+}  // namespace tn

@@ -160,22 +160,12 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* SF
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// CTA pairs (256 x 256 tiles, whole tiles only) when M > 128 and the pair tiles
-// fill at least half of the device's SM pairs; otherwise the single-CTA 128 x 128
-// instances, which also split skinny problems with stream-K.  Measured on GB300
-// (NVFP4 and MXFP8, K = 8192-16384): pairs faster from 40 tiles (1024 x 2560) up,
-// single CTAs faster at 32 tiles (512 x 4096) and 16 tiles (256 x 4096).
-bool use_pair(int64_t M, int64_t N, int sms) {
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    return M > 128 && 2 * pair_tiles >= sms / 2;
-}
-
 }  // namespace
 
 gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const void* A, const void* SFA,
                                        const void* B, const void* SFB, const void* C, void* D, int fmt,
                                        cudaStream_t stream, int sms, int dev) {
-    const bool pair = use_pair(M, N, sms);
+    const bool pair = dispatch::use_block_scaled_pair(M, N, sms);
     if (fmt == GEMM_FMT_NVFP4)
         return pair ? run<CfgNvfp4Pair>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev)
                     : run<CfgNvfp4>(M, N, K, A, SFA, B, SFB, C, D, stream, sms, dev);

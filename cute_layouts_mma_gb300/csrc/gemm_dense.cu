@@ -19,7 +19,7 @@ using CfgE5m2 = Config<KIND_FP8_E5M2, 256, 4, 2, 64, 2, 1>;
 using CfgBf16N128 = Config<KIND_BF16, 128, 6, 2, 64, 2, 1>;
 using CfgE4m3N128 = Config<KIND_FP8_E4M3, 128, 6, 2, 64, 2, 1>;
 using CfgE5m2N128 = Config<KIND_FP8_E5M2, 128, 6, 2, 64, 2, 1>;
-// Small problems (use_small_tiles): 128 x 64 tiles on single CTAs.
+// Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs.
 using CfgBf16N64 = Config<KIND_BF16, 64, 4, 2, 64, 1, 1>;
 using CfgE4m3N64 = Config<KIND_FP8_E4M3, 64, 4, 2, 64, 1, 1>;
 using CfgE5m2N64 = Config<KIND_FP8_E5M2, 64, 4, 2, 64, 1, 1>;
@@ -72,32 +72,34 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
 
 namespace {
 
-// CTA pairs when their tiles fill every SM pair (use_pairs); otherwise single CTAs:
-// 128 x 64 tiles for small problems, the 128-column instance where the 256-column one
-// would split tiles across units.
+// The instance dispatch::dense_choice picks (K coordinates per stage: 64 BF16 or
+// 128 FP8 elements).
 template <class Pair, class Single, class SingleN128, class SmallN64>
-gemm_status_t dispatch(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
-                       cudaStream_t stream, int sms, int dev) {
-    if (use_pairs(M, N, sms)) return run<Pair>(M, N, K, A, B, C, D, stream, sms, dev);
-    if (use_small_tiles<Single>(M, N, K, Single::kKCoordPerStage, sms))
-        return run<SmallN64>(M, N, K, A, B, C, D, stream, sms, dev);
-    return would_split<Single>(M, N, K, Single::kKCoordPerStage, sms)
-               ? run<SingleN128>(M, N, K, A, B, C, D, stream, sms, dev)
-               : run<Single>(M, N, K, A, B, C, D, stream, sms, dev);
+gemm_status_t dispatch_dense(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                             cudaStream_t stream, int sms, int dev) {
+    static_assert(Pair::BN == dispatch::kDensePair256.bn && Pair::PAIR == 2 && Single::BN == dispatch::kDenseSingle256.bn &&
+                      SingleN128::BN == dispatch::kDenseSingle128.bn && SmallN64::BN == dispatch::kDenseSingle64.bn,
+                  "dense tile shapes of the dispatch rules");
+    switch (dispatch::dense_choice(M, N, K, Single::kKCoordPerStage, sms)) {
+        case dispatch::DENSE_PAIR_256: return run<Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+        case dispatch::DENSE_SINGLE_64: return run<SmallN64>(M, N, K, A, B, C, D, stream, sms, dev);
+        case dispatch::DENSE_SINGLE_128: return run<SingleN128>(M, N, K, A, B, C, D, stream, sms, dev);
+        default: return run<Single>(M, N, K, A, B, C, D, stream, sms, dev);
+    }
 }
 
 }  // namespace
 
 gemm_status_t launch_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                                void* D, cudaStream_t stream, int sms, int dev) {
-    return dispatch<CfgBf16Pair, CfgBf16, CfgBf16N128, CfgBf16N64>(M, N, K, A, B, C, D, stream, sms, dev);
+    return dispatch_dense<CfgBf16Pair, CfgBf16, CfgBf16N128, CfgBf16N64>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
 gemm_status_t launch_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                               void* D, int fmt, cudaStream_t stream, int sms, int dev) {
     if (fmt == GEMM_FP8_E4M3)
-        return dispatch<CfgE4m3Pair, CfgE4m3, CfgE4m3N128, CfgE4m3N64>(M, N, K, A, B, C, D, stream, sms, dev);
-    return dispatch<CfgE5m2Pair, CfgE5m2, CfgE5m2N128, CfgE5m2N64>(M, N, K, A, B, C, D, stream, sms, dev);
+        return dispatch_dense<CfgE4m3Pair, CfgE4m3, CfgE4m3N128, CfgE4m3N64>(M, N, K, A, B, C, D, stream, sms, dev);
+    return dispatch_dense<CfgE5m2Pair, CfgE5m2, CfgE5m2N128, CfgE5m2N64>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
 unsigned int read_clear_error_dense() { return read_clear_word(g_err_dense); }

@@ -5,7 +5,7 @@
 
 namespace tn {
 
-// CTA pairs (use_pairs): 256 x 256 tiles, 6 stages of 64 K, two TMEM accumulators,
+// CTA pairs (dispatch::use_pairs): 256 x 256 tiles, 6 stages of 64 K, two TMEM accumulators,
 // epilogue staged in 32 x 64 chunks (128-byte rows), double-buffered.
 using CfgF16Acc32Pair = Config<KIND_F16_ACC32, 256, 6, 2, 64, 2, 2>;
 using CfgF16Acc16Pair = Config<KIND_F16_ACC16, 256, 6, 2, 64, 2, 2>;
@@ -16,7 +16,7 @@ using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
 // accumulation): 128-column tiles, so stream-K cuts each tile into fewer, smaller
 // pieces.
 using CfgF16N128 = Config<KIND_F16_ACC32, 128, 6, 2, 64, 2, 1>;
-// Small problems (use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages, each
+// Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages, each
 // epilogue warp staging its whole 32 x 64 slice.
 using CfgF16N64 = Config<KIND_F16_ACC32, 64, 4, 2, 64, 1, 1>;
 // Narrow K (fp32 accumulation): a whole K of at most 32 or 16 elements fits a 64- or
@@ -28,6 +28,12 @@ using CfgF16K32Pair = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 2, 4, 64>;
 using CfgF16K32 = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 1, 4, 64>;
 using CfgF16K16Pair = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 2, 4, 32>;
 using CfgF16K16 = Config<KIND_F16_ACC32, 256, 6, 2, 64, 4, 1, 4, 32>;
+
+// The instances behind dispatch::dense_choice.
+static_assert(dispatch::kDensePair256.bn == CfgF16Acc32Pair::BN && dispatch::kDensePair256.pair == CfgF16Acc32Pair::PAIR &&
+                  dispatch::kDenseSingle256.bn == CfgF16Acc32::BN && dispatch::kDenseSingle128.bn == CfgF16N128::BN &&
+                  dispatch::kDenseSingle64.bn == CfgF16N64::BN && CfgF16Acc32::kStreamK && CfgF16N128::kStreamK,
+              "dense tile shapes of the dispatch rules");
 
 // Device-side record of an abandoned launch (a bounded wait ran out).
 static __device__ unsigned int g_err_f16;
@@ -85,7 +91,6 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
 
 gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                               void* D, int accum, cudaStream_t stream, int sms, int dev) {
-    const bool pair = use_pairs(M, N, sms);
     if (accum == GEMM_ACC_F32) {
         // narrow K: bound by the C and D traffic, pairs whenever M > 128
         if (K <= 16)
@@ -94,13 +99,15 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
         if (K <= 32)
             return M > 128 ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                            : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
-        if (pair) return run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
-        if (use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms)) return run<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
-        return would_split<CfgF16Acc32>(M, N, K, 64, sms) ? run<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev)
-                                                           : run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+        switch (dispatch::dense_choice(M, N, K, 64, sms)) {
+            case dispatch::DENSE_PAIR_256: return run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+            case dispatch::DENSE_SINGLE_64: return run<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
+            case dispatch::DENSE_SINGLE_128: return run<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev);
+            default: return run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+        }
     }
-    return pair ? run<CfgF16Acc16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
-                : run<CfgF16Acc16>(M, N, K, A, B, C, D, stream, sms, dev);
+    return dispatch::use_pairs(M, N, sms) ? run<CfgF16Acc16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                                          : run<CfgF16Acc16>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -148,11 +155,12 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const 
 gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                                       void* D, cudaStream_t stream, int sms, int dev) {
     // the same instance choice as gemm_f16 with fp32 accumulation and K > 32
-    if (use_pairs(M, N, sms)) return run_noalloc<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
-    if (use_small_tiles<CfgF16Acc32>(M, N, K, 64, sms))
-        return run_noalloc<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
-    return would_split<CfgF16Acc32>(M, N, K, 64, sms) ? run_noalloc<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev)
-                                                       : run_noalloc<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+    switch (dispatch::dense_choice(M, N, K, 64, sms)) {
+        case dispatch::DENSE_PAIR_256: return run_noalloc<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
+        case dispatch::DENSE_SINGLE_64: return run_noalloc<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
+        case dispatch::DENSE_SINGLE_128: return run_noalloc<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev);
+        default: return run_noalloc<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+    }
 }
 
 unsigned int read_clear_error_f16() { return read_clear_word(g_err_f16); }

@@ -6,20 +6,11 @@
 #include <cstdint>
 #include <mutex>
 
+#include "dispatch.h"
 #include "gemm_kernel.cuh"
 #include "launch.h"
 
 namespace tn {
-
-// Stream-K is used when whole tiles would leave more than three quarters of the
-// units idle, each unit's share is at least kStreamKMinShare k-blocks, and the
-// accumulation is fp32.  Outside that range, measurement on GB300 favoured whole
-// tiles: once a quarter of the SMs stream operands, skinny problems are bound by
-// HBM rather than by SM count; dense FP16 runs at the power limit, where idle SMs
-// raise the clock of the busy ones; and short shares leave each split tile in many
-// pieces whose partials the finishing unit adds one after another.
-constexpr double kStreamKMinIdle = 0.75;
-constexpr long long kStreamKMinShare = 12;
 
 // Scratch of a stream-K launch: fp32 partial sums and per-warp flags.
 template <class Cfg>
@@ -66,64 +57,18 @@ struct LaunchState {
 template <class Cfg>
 std::atomic<int> LaunchState<Cfg>::max_units[kMaxDevices];
 
-// Schedule of one launch: units used and how many tiles (the last ones) are split.
-struct Schedule {
-    int units;
-    int sk_tiles;
-};
+using dispatch::Schedule;
+
+// The schedule-relevant shape of an instance.
+template <class Cfg>
+constexpr dispatch::TileShape tile_shape() {
+    return dispatch::TileShape{Cfg::BM_TILE, Cfg::BN, Cfg::PAIR, Cfg::kStreamK};
+}
 
 template <class Cfg>
 Schedule choose_schedule(const Params& p, int max_units) {
-    const long long tiles = static_cast<long long>(p.num_m_blocks) * p.num_n_blocks;
-    Schedule sc{static_cast<int>(tiles < max_units ? tiles : max_units), 0};
-    if (!Cfg::kStreamK) return sc;
-    const long long rounds = (tiles + max_units - 1) / max_units;
-    const double idle = 1.0 - static_cast<double>(tiles) / static_cast<double>(rounds * max_units);
-    if (idle <= kStreamKMinIdle) return sc;
-    const long long split = tiles % max_units;  // the tiles of the last, partly idle round
-    if (split * p.num_k_blocks < kStreamKMinShare * max_units) return sc;
-    return Schedule{max_units, static_cast<int>(split)};
-}
-
-// Launch configuration shared by every launch of Cfg: block, shared memory, stream,
-// the (2,1,1) cluster of CTA pairs.  On first use per device it sets the kernel's
-// shared-memory attribute and finds the units (resident CTAs, or clusters for
-// PAIR = 2) the device keeps at once.
-// Whether Cfg's own schedule would split tiles for this problem (units estimated
-// as one per SM, or one per SM pair).  The launchers then switch to their
-// 128-column instance: half as many pieces per split tile and half the partial
-// bytes per piece, which measured 1.2-1.8x faster on such skinny problems.
-template <class Cfg>
-bool would_split(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
-    Params q{};
-    q.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
-    q.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
-    q.num_k_blocks = static_cast<int>((K + k_per_block - 1) / k_per_block);
-    return choose_schedule<Cfg>(q, Cfg::PAIR == 2 ? sms / 2 : sms).sk_tiles != 0;
-}
-
-// Dense kinds: CTA pairs (256 x 256 tiles) once their tiles fill every SM pair at least
-// once; below that the single-CTA instances (128 x 256, or 128 x 128 with stream-K, or
-// 128 x 64) spread the work over twice as many units.  Measured on GB300 (FP16, no C):
-// 512 x 8192 x 2048 14.5 -> 13.7 us, 2048^2 x 1024 10.0 -> 9.1, 256 x 2048 x 8192
-// 26.5 -> 22.7; 4096^2 x 1024 (256 pair tiles) stays on pairs (24.0 against 26.5).
-inline bool use_pairs(int64_t M, int64_t N, int sms) {
-    return M > 128 && ((M + 255) / 256) * ((N + 255) / 256) >= sms / 2;
-}
-
-// Small problems: whole tiles of `Big` (256 columns; CTA pairs for M > 128) would keep
-// fewer than half of the units busy, K is short (at most 1024) and no stream-K split
-// applies.  Such a launch is bound by each CTA's operand loads and its fixed latency,
-// so the launchers switch to 128 x 64 tiles on single CTAs: many more CTAs, each
-// loading a fraction of the bytes (FP16 256^3: 5.3 -> 3.7 us per call on GB300).
-// Long K keeps the big tiles: an N = 64 MMA is too short for the single issuing
-// thread to keep the tensor pipe busy.
-template <class Big>
-bool use_small_tiles(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
-    if (K > 1024) return false;
-    const int64_t tiles = ((M + Big::BM_TILE - 1) / Big::BM_TILE) * ((N + Big::BN - 1) / Big::BN);
-    const int units = Big::PAIR == 2 ? sms / 2 : sms;
-    return 2 * tiles < units && !would_split<Big>(M, N, K, k_per_block, sms);
+    return dispatch::choose_schedule(static_cast<long long>(p.num_m_blocks) * p.num_n_blocks, p.num_k_blocks,
+                                     max_units, Cfg::kStreamK);
 }
 
 template <class Cfg>
