@@ -26,8 +26,9 @@
 //                whatever the box size, so each operand stream has its own warp.
 //   warps 3, 12  (block-scaled only) issuers of the raw scale boxes (this CTA's
 //                128 SFA rows, all BN SFB rows of the tile) on `sf_full`: TMA boxes
-//                of the row-major scales, or (NVFP4) bulk copies of packed blocks.
-//                In the register-drain layout warp 3 issues both.
+//                of the row-major scales, or (NVFP4, and MXFP8 in CTA pairs) bulk
+//                copies of packed blocks.  In the register-drain layout warp 3 issues
+//                both.
 //   warp 1       TMEM allocation; in the leader, the MMA issuer (one thread):
 //                tcgen05.mma into a TMEM accumulator, 32 bytes of K per MMA;
 //                tcgen05.commit frees the stage (`empty`, in both CTAs) and, at the
@@ -50,7 +51,7 @@
 //                `full` barrier of the stage, so that the MMA issuer waits on one
 //                barrier per stage (a second wait per stage costs the single issuing
 //                thread ~200 cycles of its 512-cycle stage).
-// Register-drain layout (NVFP4 CTA pairs): 512 threads, four warpgroups -- 0-3
+// Register-drain layout (NVFP4 and MXFP8 CTA pairs): 512 threads, four warpgroups -- 0-3
 // issuers and MMA, 4-7 epilogue, 8-11 scale writers, 12-15 epilogue.  setmaxnreg
 // moves registers from the first and third to the epilogue warpgroups, so that an
 // epilogue warp holds its whole 32 x 128 slice of the accumulator at once.
@@ -205,8 +206,9 @@ struct Config {
     static_assert(kRegsIssue + kRegsWriter + 2 * kRegsEpi == 4 * 128, "register split adds up to the launch's");
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
-    // NVFP4 stages and MXFP8 CTA-pair stages read their scales from packed 2 KB
-    // blocks (one bulk copy per 128 rows; an MXFP8 block serves four stages).  The
+    // NVFP4 stages and MXFP8 CTA-pair stages read their scales from packed blocks
+    // (one bulk copy per row group: SFA 128 rows, SFB one tile's BN rows; an MXFP8
+    // block serves four stages).  The
     // single-CTA MXFP8 instance, whose skinny problems would pay the regrouping pass
     // on top of a short, memory-bound GEMM, keeps the TMA boxes.
     static constexpr bool kPackedScales = KIND == KIND_NVFP4 || (KIND == KIND_MXFP8 && PAIR == 2);
