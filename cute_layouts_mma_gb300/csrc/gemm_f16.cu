@@ -112,8 +112,9 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
 
 // ---------------------------------------------------------------- no-allocation variant
 // Scratch of gemm_f16_noalloc: one fixed block per device, part of the loaded
-// module, so the call never allocates.  20 MiB holds the stream-K partials and
-// flags of a device with up to 159 SMs (a 152-SM GB300 needs 19.0 MiB).  Every
+// module, so the call never allocates.  20 MiB holds the stream-K partials (128 x 128
+// single-CTA tiles: 64 KB per SM) and flags of a device with up to 319 SMs (a 152-SM
+// GB300 needs 9.5 MiB).  Every
 // call shares it: calls that overlap on the GPU would overwrite each other's
 // partials and flags.
 constexpr size_t kStaticScratchBytes = size_t(20) << 20;

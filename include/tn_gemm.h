@@ -19,8 +19,8 @@
  *   - Scratch: when the output tiles do not fill whole rounds of the device's
  *     SMs, fp32 accumulation uses a stream-K schedule (units split the k-blocks
  *     of the tiles evenly; a tile cut between units is summed through fp32
- *     partials in scratch memory).  That scratch (128 KB per SM at most, about
- *     19.5 MB on 152 SMs) is taken with cudaMallocFromPoolAsync on `stream`
+ *     partials in scratch memory).  That scratch (64 KB per SM at most, about
+ *     9.5 MiB on 152 SMs) is taken with cudaMallocFromPoolAsync on `stream`
  *     from a per-device memory pool the library creates on first need, and
  *     returned to the pool with cudaFreeAsync on `stream` after the kernel; the
  *     pool keeps its memory for later calls until the process exits.  NVFP4
@@ -151,11 +151,11 @@ gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void *A, const voi
  *     call on a device looks up the block's device address there (once per
  *     device, with that device current); make that first call before any
  *     stream capture.
- *   - A stream-K launch needs 128 KB of fp32 partials per SM it runs on, plus
- *     flags: 19.0 MiB on a 152-SM GB300.  A launch whose need exceeds the 20 MiB
- *     block (a device of more than 159 SMs) is refused with
- *     GEMM_ERR_INVALID_ARG and nothing is enqueued.  Whole-tile launches use no
- *     scratch.
+ *   - A stream-K launch (128 x 128 tiles on single CTAs) needs 64 KB of fp32
+ *     partials per SM it runs on, plus flags: 9.5 MiB on a 152-SM GB300.  A
+ *     launch whose need exceeds the 20 MiB block (a device of more than 319
+ *     SMs) is refused with GEMM_ERR_INVALID_ARG and nothing is enqueued.
+ *     Whole-tile launches use no scratch.
  *   - Every call on a device shares the block and it keeps the last call's
  *     contents: each call clears the flags it uses (an async memset on
  *     `stream`); partial sums are written before they are read.  Calls that
