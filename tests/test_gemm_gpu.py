@@ -186,9 +186,13 @@ def test_one_hot_scale_probe(kind, row, col, sfk, M, N, K):
 
 @pytest.mark.parametrize("kind", ["nvfp4", "mxfp8"])
 @pytest.mark.parametrize("with_c", [False, True])
-def test_block_scaled_pair_integers_bit_exact(kind, with_c):
-    # 1000 x 2504: 40 tiles of 256 x 256 (CTA-pair instance), ragged in M and N
-    prob = inputs.make_problem(kind, 1000, 2504, 512, seed=15, dist="int", with_c=with_c)
+@pytest.mark.parametrize("kmul", [1, 4])
+def test_block_scaled_pair_integers_bit_exact(kind, with_c, kmul):
+    # 1000 x 2504: 40 tiles of 256 x 256 (CTA-pair instance), ragged in M and N; the
+    # smallest legal K (NVFP4 256: one stage; MXFP8 512: four stages, one scale column)
+    # and four times that
+    K = (256 if kind == "nvfp4" else 512) * kmul
+    prob = inputs.make_problem(kind, 1000, 2504, K, seed=15 + kmul, dist="int", with_c=with_c)
     P.check(prob, P.run_gpu(prob), mode="exact")
 
 
