@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(PackJob a, PackJob b, 
     const size_t pitch = static_cast<size_t>(cols16) * 16;
     uint4* out = reinterpret_cast<uint4*>(j.dst + static_cast<size_t>(blk) * j.group_rows * 16);
     for (int r = lane; r < j.group_rows; r += 32) {
-        const int row = g * j.group_rows + r;
+        const long long row = static_cast<long long>(g) * j.group_rows + r;  // may pass INT_MAX near M = 2^31
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (row < j.rows) v = __ldg(reinterpret_cast<const uint4*>(j.src + static_cast<size_t>(row) * pitch + 16 * c));
         out[r] = v;
