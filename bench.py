@@ -1,6 +1,6 @@
 """Benchmark of the GB300 TN GEMM (one JSON line on rank 0).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference|vendor]
 
 A step is one GEMM over one synthetic problem of the named workload (default:
 the FP16 M=N=K=4096 GEMM with fp32 accumulation and C).  Inputs live in HBM before
@@ -12,6 +12,9 @@ slowest rank's time.
 
 --impl reference times the CPU oracle (the deliberately slow fp64 reference) on
 a bounded row sample of the same workload per step, on the host cores.
+
+--impl vendor times the vendor library (cuBLAS through torch) on the same workload,
+for context (one GPU, a short JSON line with "impl": "vendor").
 """
 from __future__ import annotations
 
@@ -189,6 +192,93 @@ class GemmRunner:
             self.tg.gemm_fp8(s["A"], s["B"], s["C"], s["D"], self.fmt, stream)
         else:
             self.tg.gemm_block_scaled(s["A"], s["SFA"], s["B"], s["SFB"], s["C"], s["D"], self.fmt, stream)
+
+
+def vendor_blocked_scales(sf):
+    """Row-major scales [rows][cols] (u8) in the vendor library's blocked order: 128-row x
+    4-column blocks, row-block major, each block 512 bytes with scale (r, c) at byte
+    16 * (r % 32) + 4 * (r // 32) + c -- the 32-lane base tile of the TMEM scale placement
+    (local_lane = r % 32, TCol = r // 32, byte = c).  Rows and columns are zero-padded."""
+    import torch
+    rows, cols = sf.shape
+    rb, cb = (rows + 127) // 128, (cols + 3) // 4
+    padded = torch.zeros(rb * 128, cb * 4, dtype=sf.dtype, device=sf.device)
+    padded[:rows, :cols] = sf
+    return padded.view(rb, 4, 32, cb, 4).permute(0, 3, 2, 1, 4).contiguous().flatten()
+
+
+class VendorRunner:
+    """The same workload through the vendor library (cuBLAS via torch), for context only.
+    Block-scaled calls take their scales in the vendor's blocked order (converted once,
+    outside timing); its block-scaled and FP8 calls add no C."""
+
+    def __init__(self, w, dev, sets: int):
+        import torch
+        from cute_layouts_mma_gb300 import inputs
+        self.w = w
+        base = inputs.make_problem(w.kind, w.M, w.N, w.K, w.seed, w.dist, w.with_c)
+        out_dtype = torch.float16 if w.kind == "f16" else torch.bfloat16
+        self.sets = []
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        for i in range(sets):
+            s = {"D": torch.empty(w.M, w.N, dtype=out_dtype, device=dev), "one": one}
+            if w.kind in ("f16", "bf16"):
+                s["A"], s["B"] = base["A"].to(dev), base["B"].to(dev)
+                s["C"] = base["C"].to(dev) if base.get("C") is not None else None
+            elif w.kind in ("fp8e4m3", "fp8e5m2"):
+                dt = torch.float8_e4m3fn if w.kind == "fp8e4m3" else torch.float8_e5m2
+                s["A"], s["B"] = base["A"].to(dev).view(dt), base["B"].to(dev).view(dt)
+            else:
+                dt = torch.float4_e2m1fn_x2 if w.kind == "nvfp4" else torch.float8_e4m3fn
+                sdt = torch.float8_e4m3fn if w.kind == "nvfp4" else torch.float8_e8m0fnu
+                s["A"], s["B"] = base["A"].to(dev).view(dt), base["B"].to(dev).view(dt)
+                s["SFA"] = vendor_blocked_scales(base["SFA"].to(dev)).view(sdt)
+                s["SFB"] = vendor_blocked_scales(base["SFB"].to(dev)).view(sdt)
+            self.sets.append(s)
+
+    def launch(self, i: int, stream=None):
+        import torch
+        s = self.sets[i % len(self.sets)]
+        if self.w.kind in ("f16", "bf16"):
+            if s["C"] is not None:
+                torch.addmm(s["C"], s["A"], s["B"].t(), out=s["D"])
+            else:
+                torch.mm(s["A"], s["B"].t(), out=s["D"])
+        elif self.w.kind in ("fp8e4m3", "fp8e5m2"):
+            torch._scaled_mm(s["A"], s["B"].t(), s["one"], s["one"], out_dtype=torch.bfloat16, out=s["D"])
+        else:
+            torch._scaled_mm(s["A"], s["B"].t(), s["SFA"], s["SFB"], out_dtype=torch.bfloat16, out=s["D"])
+
+
+def vendor_arm(args):
+    """Times the vendor library on the workload (context for the tables, not a bench line)."""
+    import torch
+    w = __import__("cute_layouts_mma_gb300.inputs", fromlist=["WORKLOADS"]).WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if w.kind == "f16" and w.accum == 1:
+        print(json.dumps({"impl": "vendor", "workload": w.name, "unavailable": "no fp16-accumulate GEMM in torch"}))
+        return
+    runner = VendorRunner(w, dev, rotating_sets(w))
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            runner.launch(i)
+    torch.cuda.synchronize()
+    if args.quick:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                runner.launch(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"impl": "vendor", "quick": True, "workload": w.name}), flush=True)
+        return
+    peaks, peak_src = load_peaks()
+    with ClockSampler(0) as clocks:
+        ms = time_steps(runner, args.steps, stream, graph=not args.no_graph) / args.steps
+    print(json.dumps({"impl": "vendor", "workload": w.name, "ms_per_step": round(ms, 5),
+                      "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2), "roofline": roofline(w, ms, peaks, peak_src),
+                      "clocks": clocks.summary(),
+                      "note": "cuBLAS through torch; block-scaled and FP8 calls add no C"}), flush=True)
 
 
 def rotating_sets(w) -> int:
@@ -543,7 +633,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="fp16_4096")
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--impl", choices=["ours", "reference", "vendor"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
@@ -558,6 +648,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         reference_arm(args)
+    elif args.impl == "vendor":
+        vendor_arm(args)
     else:
         gpu_arm(args)
 

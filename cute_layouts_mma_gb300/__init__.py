@@ -50,9 +50,15 @@ _lib = None
 _lock = threading.Lock()
 
 
+# Test builds only (cute_layouts_mma_gb300/build.py VARIANTS): a test process may set
+# TN_GEMM_TEST_VARIANT before the first call to run the same calls on a test build of
+# the library, e.g. "scale_copy" (block-scaled scales moved with tcgen05.cp).
+_TEST_VARIANT_ENV = "TN_GEMM_TEST_VARIANT"
+
+
 def library_path() -> str:
     from . import build as _b
-    return _b.LIB
+    return _b.lib_path(os.environ.get(_TEST_VARIANT_ENV, ""))
 
 
 def lib() -> ctypes.CDLL:
@@ -62,7 +68,10 @@ def lib() -> ctypes.CDLL:
         with _lock:
             if _lib is None:
                 from . import build as _b
-                path = _b.build()
+                variant = os.environ.get(_TEST_VARIANT_ENV, "")
+                if variant and variant not in _b.VARIANTS:
+                    raise ValueError(f"{_TEST_VARIANT_ENV}={variant!r} is not a test build of this library")
+                path = _b.build(variant=variant)
                 l = ctypes.CDLL(path)
                 i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
                 l.gemm_f16.argtypes = [i64, i64, i64, vp, vp, vp, vp, ci, vp]
@@ -132,12 +141,13 @@ def gemm_f16(A, B, C, D, accum_dtype: int = GEMM_ACC_F32, stream=None) -> None:
 
 
 def gemm_f16_noalloc(A, B, C, D, stream=None) -> None:
-    """gemm_f16 with fp32 accumulation whose scratch is the library's fixed block.
+    """gemm_f16 with fp32 accumulation on the stream-K schedule, whose scratch is the
+    library's fixed device block (no allocation).
 
-    For callers that must not allocate device memory during the call (the
-    library's own pool included).  Calls that overlap on the GPU share the block
-    and race: keep them ordered on one stream.  Make the first call on a device
-    outside any stream capture (it looks up the block's address).
+    For callers that must not allocate device memory during the call.  Calls that
+    overlap on the GPU share the block and race: keep them ordered on one stream.
+    The first accepted call of the library on a device loads the block and looks up
+    its address: make it before reserving the device's memory or capturing a stream.
     """
     import torch
     M, K = A.shape

@@ -18,9 +18,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtn_gemm.so")
-# Test-only variant: compiled with TN_TIMEOUT_INJECT, one pipeline arrival is
-# withheld so that a bounded wait runs out (exercises the abandon path).
-VARIANTS = {"timeout_inject": ["-DTN_TIMEOUT_INJECT"]}
+# Test-only variants.  timeout_inject: one pipeline arrival is withheld so that a
+# bounded wait runs out (exercises the abandon path).  scale_copy: the block-scaled
+# instances move their scales with tcgen05.cp instead of tcgen05.st (the pages' copy
+# instruction, kept as a tested compile-time alternative).
+VARIANTS = {"timeout_inject": ["-DTN_TIMEOUT_INJECT"], "scale_copy": ["-DTN_SCALE_COPY"]}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -45,6 +45,13 @@ gemm_status_t device_info(int* dev, int* sms) {
         cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
+    // First accepted call on this device: load the module block of gemm_f16_noalloc
+    // now (lazy module loading would otherwise defer it to that call's first use).
+    static std::atomic<bool> ready[kMaxDevices];
+    if (!ready[*dev].load(std::memory_order_acquire)) {
+        if (!setup_fixed_scratch(*dev)) return GEMM_ERR_CUDA;
+        ready[*dev].store(true, std::memory_order_release);
+    }
     return GEMM_OK;
 }
 
@@ -96,27 +103,6 @@ bool encode_tma_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
     cache_next = (cache_next + 1) % kEntries;
     if (cache_used < kEntries) ++cache_used;
     return true;
-}
-
-namespace {
-std::mutex g_pool_mutex;
-cudaMemPool_t g_pools[kMaxDevices] = {};
-}  // namespace
-
-cudaMemPool_t scratch_pool(int dev) {
-    std::lock_guard<std::mutex> lock(g_pool_mutex);
-    if (g_pools[dev] == nullptr) {
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        cudaMemPool_t pool = nullptr;
-        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
-        uint64_t keep = UINT64_MAX;  // keep the memory in the pool between calls
-        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-        g_pools[dev] = pool;
-    }
-    return g_pools[dev];
 }
 
 }  // namespace tn

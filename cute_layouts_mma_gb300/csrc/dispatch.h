@@ -88,15 +88,102 @@ enum DenseChoice { DENSE_PAIR_256 = 0, DENSE_SINGLE_256 = 1, DENSE_SINGLE_128 = 
 
 // CTA pairs when their tiles fill every SM pair; otherwise single CTAs: 128 x 64 tiles
 // for small problems, the 128-column instance where the 256-column one would split.
+// (The stream-K rule of the fixed-scratch call; dense_plan below is the rule of the
+// calls that split tiles inside clusters.)
 inline DenseChoice dense_choice(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
     if (use_pairs(M, N, sms)) return DENSE_PAIR_256;
     if (use_small_tiles(M, N, K, k_per_block, sms, kDenseSingle256)) return DENSE_SINGLE_64;
     return would_split(M, N, K, k_per_block, sms, kDenseSingle256) ? DENSE_SINGLE_128 : DENSE_SINGLE_256;
 }
 
+// ------------------------------------------------------------------ cluster split
+// A problem whose whole tiles fit one round of the device but leave more than half
+// of its SMs idle gives each tile to a cluster of s single CTAs (s <= kMaxSplit, the
+// portable cluster size): CTA r of the cluster sums k-blocks [r*nkb/s, (r+1)*nkb/s)
+// of the tile, and the cluster adds its s fp32 partials through distributed shared
+// memory.  The split is the largest s that keeps every CTA at least kSplitMinShare
+// k-blocks, puts at most one CTA on each SM, and lets every tile's cluster be
+// resident at once (resident[s]: co-resident clusters of s CTAs of the instance).
+constexpr int kMaxSplit = 8;
+constexpr int kSplitMinShare = 4;
+constexpr double kSplitMinIdle = 0.5;
+
+inline int choose_split(long long tiles, int nkb, int sms, const int* resident) {
+    if (tiles <= 0 || tiles > sms) return 1;
+    if (1.0 - static_cast<double>(tiles) / sms <= kSplitMinIdle) return 1;
+    int best = 1;
+    for (int s = 2; s <= kMaxSplit; ++s) {
+        if (static_cast<long long>(nkb) < static_cast<long long>(s) * kSplitMinShare) break;
+        if (tiles * s > sms) break;
+        if (tiles <= resident[s]) best = s;
+    }
+    return best;
+}
+
+// Operand bytes one CTA of a single-CTA instance loads per k-block (128 bytes of K per
+// operand row), and the fp32 partial tile a cluster split adds up.
+inline long long kblock_bytes(int bn) { return 128LL * (128 + bn); }
+inline long long partial_bytes(int bn) { return 128LL * bn * 4; }
+
+// Estimated per-SM bytes of a single-CTA plan: the operand bytes of every round of
+// whole tiles (or of one CTA's share of a split tile), plus, for a split, the partial
+// tile written and read back through shared memory.  Single-CTA tiles are bound by
+// the bytes each SM pulls from L2, so the plan with the fewest bytes per SM is taken.
+inline long long plan_bytes(long long tiles, int nkb, int bn, int split, int sms) {
+    if (split > 1) return ((nkb + split - 1) / split) * kblock_bytes(bn) + partial_bytes(bn);
+    const long long rounds = (tiles + sms - 1) / sms;
+    return rounds * nkb * kblock_bytes(bn);
+}
+
+struct DensePlan {
+    DenseChoice choice;
+    int split;  // cluster size of the split (1 = whole tiles)
+};
+
+// The dense instance and split for a problem: CTA pairs when their tiles fill every SM
+// pair; 128 x 64 single-CTA tiles for small problems (K <= 1024 and the 128 x 256 tiles
+// would keep fewer than half of the SMs busy: 1024^3 FP16 7.0 us against 12.6 us split
+// in clusters); otherwise whichever of the
+// 128 x 256 and 128 x 128 single-CTA instances, each with its own cluster split,
+// moves the fewest bytes per SM (ties: the wider tile).  res256 / res128: resident
+// clusters per cluster size of the two instances.
+inline DensePlan dense_plan(int64_t M, int64_t N, int64_t K, int k_per_block, int sms, const int* res256,
+                            const int* res128) {
+    if (use_pairs(M, N, sms)) return DensePlan{DENSE_PAIR_256, 1};
+    const int nkb = static_cast<int>((K + k_per_block - 1) / k_per_block);
+    const long long t256 = tile_count(M, N, kDenseSingle256), t128 = tile_count(M, N, kDenseSingle128);
+    const int s256 = choose_split(t256, nkb, sms, res256);
+    const int s128 = choose_split(t128, nkb, sms, res128);
+    if (K <= 1024 && 2 * t256 < sms) return DensePlan{DENSE_SINGLE_64, 1};
+    const long long b256 = plan_bytes(t256, nkb, 256, s256, sms), b128 = plan_bytes(t128, nkb, 128, s128, sms);
+    return b128 < b256 ? DensePlan{DENSE_SINGLE_128, s128} : DensePlan{DENSE_SINGLE_256, s256};
+}
+
+// ------------------------------------------------------------------ tile raster
+// m blocks per raster group (tiles run down a group of m blocks, column by column): the
+// largest group, up to kRasterMaxGroup, whose A panels, plus the B panels one wave of
+// `units` tiles touches, fit in `budget` bytes of L2.  Then each A panel is read from
+// memory about once and each B panel once per group.  a_panel / b_panel: bytes of one
+// tile-row of A (and its scales) over the whole K, and of one tile-column of B.  The cap:
+// a group of 32 (every m block of NVFP4 8192^3 at once) put 32 concurrent tiles on each
+// B panel and ran 188 us against 185 us with 8 or 16 on GB300.
+constexpr long long kRasterL2Budget = 64LL << 20;
+constexpr int kRasterMaxGroup = 16;
+
+inline int raster_group(long long num_m, long long num_n, long long units, long long a_panel, long long b_panel,
+                        long long budget = kRasterL2Budget) {
+    int best = 1;
+    for (long long g = 1; g <= num_m && g <= kRasterMaxGroup; ++g) {
+        const long long wave = units < g * num_n ? units : g * num_n;
+        const long long cols = (wave + g - 1) / g + 1;
+        if (g * a_panel + cols * b_panel <= budget) best = static_cast<int>(g);
+    }
+    return best;
+}
+
 // Block-scaled kinds: CTA pairs (256 x 256 tiles, whole tiles only) when M > 128 and the
 // pair tiles fill at least half of the device's SM pairs; otherwise the single-CTA
-// 128 x 128 instances, which also split skinny problems with stream-K.  Measured on
+// 128 x 128 instances, which also split skinny problems inside clusters.  Measured on
 // GB300 (NVFP4 and MXFP8, K = 8192-16384): pairs faster from 40 tiles (1024 x 2560) up,
 // single CTAs faster at 32 tiles (512 x 4096) and 16 tiles (256 x 4096).
 inline bool use_block_scaled_pair(int64_t M, int64_t N, int sms) {

@@ -15,7 +15,7 @@ using CfgE4m3Pair = Config<KIND_FP8_E4M3, 256, 6, 2, 64, 2, 2>;
 using CfgE4m3 = Config<KIND_FP8_E4M3, 256, 4, 2, 64, 2, 1>;
 using CfgE5m2Pair = Config<KIND_FP8_E5M2, 256, 6, 2, 64, 2, 2>;
 using CfgE5m2 = Config<KIND_FP8_E5M2, 256, 4, 2, 64, 2, 1>;
-// Skinny problems that the 256-column instances would split: 128-column tiles (as FP16).
+// Skinny problems: 128-column tiles where they move fewer bytes per SM (as FP16).
 using CfgBf16N128 = Config<KIND_BF16, 128, 6, 2, 64, 2, 1>;
 using CfgE4m3N128 = Config<KIND_FP8_E4M3, 128, 6, 2, 64, 2, 1>;
 using CfgE5m2N128 = Config<KIND_FP8_E5M2, 128, 6, 2, 64, 2, 1>;
@@ -35,7 +35,7 @@ unsigned int* err_word(int dev) { return device_symbol(g_err_dense, g_err_addr, 
 
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
-                  cudaStream_t stream, int sms, int dev) {
+                  cudaStream_t stream, int sms, int dev, int split = 1) {
     constexpr bool k16 = operands_16bit(Cfg::KIND);
     const CUtensorMapDataType in_type = k16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const uint64_t row_bytes = static_cast<uint64_t>(K) * (k16 ? 2 : 1);
@@ -54,7 +54,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
         return GEMM_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (err == nullptr) return GEMM_ERR_CUDA;
-    Params p;
+    Params p{};
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -64,6 +64,7 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
     p.C = C;
     p.D = D;
     p.err = err;
+    p.split = split;
     if (launch_config<Cfg>(ta, tb, ta, tb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -72,19 +73,24 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
 
 namespace {
 
-// The instance dispatch::dense_choice picks (K coordinates per stage: 64 BF16 or
-// 128 FP8 elements).
+// The instance and cluster split dispatch::dense_plan picks (K coordinates per stage:
+// 64 BF16 or 128 FP8 elements).
 template <class Pair, class Single, class SingleN128, class SmallN64>
 gemm_status_t dispatch_dense(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
                              cudaStream_t stream, int sms, int dev) {
     static_assert(Pair::BN == dispatch::kDensePair256.bn && Pair::PAIR == 2 && Single::BN == dispatch::kDenseSingle256.bn &&
                       SingleN128::BN == dispatch::kDenseSingle128.bn && SmallN64::BN == dispatch::kDenseSingle64.bn,
                   "dense tile shapes of the dispatch rules");
-    switch (dispatch::dense_choice(M, N, K, Single::kKCoordPerStage, sms)) {
+    int res256[dispatch::kMaxSplit + 1], res128[dispatch::kMaxSplit + 1];
+    if (split_capacity<Single>(sms, dev, res256) != cudaSuccess ||
+        split_capacity<SingleN128>(sms, dev, res128) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const dispatch::DensePlan plan = dispatch::dense_plan(M, N, K, Single::kKCoordPerStage, sms, res256, res128);
+    switch (plan.choice) {
         case dispatch::DENSE_PAIR_256: return run<Pair>(M, N, K, A, B, C, D, stream, sms, dev);
         case dispatch::DENSE_SINGLE_64: return run<SmallN64>(M, N, K, A, B, C, D, stream, sms, dev);
-        case dispatch::DENSE_SINGLE_128: return run<SingleN128>(M, N, K, A, B, C, D, stream, sms, dev);
-        default: return run<Single>(M, N, K, A, B, C, D, stream, sms, dev);
+        case dispatch::DENSE_SINGLE_128: return run<SingleN128>(M, N, K, A, B, C, D, stream, sms, dev, plan.split);
+        default: return run<Single>(M, N, K, A, B, C, D, stream, sms, dev, plan.split);
     }
 }
 

@@ -12,9 +12,8 @@ using CfgF16Acc16Pair = Config<KIND_F16_ACC16, 256, 6, 2, 64, 2, 2>;
 // Single CTAs: 128 x 256 tiles, 4 stages.
 using CfgF16Acc32 = Config<KIND_F16_ACC32, 256, 4, 2, 64, 2, 1>;
 using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
-// Skinny problems whose 256-column tiles would leave most units idle (fp32
-// accumulation): 128-column tiles, so stream-K cuts each tile into fewer, smaller
-// pieces.
+// Skinny problems (fp32 accumulation): 128-column tiles where they move fewer bytes
+// per SM than 128 x 256 ones (each instance with its own cluster split).
 using CfgF16N128 = Config<KIND_F16_ACC32, 128, 6, 2, 64, 2, 1>;
 // Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages, each
 // epilogue warp staging its whole 32 x 64 slice.
@@ -48,6 +47,7 @@ unsigned int* err_word(int dev) { return device_symbol(g_err_f16, g_err_addr, de
 template <class Cfg>
 gemm_status_t prepare(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
                       int dev, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& td, CUtensorMap& tc, Params& p) {
+    p = Params{};
     // A: fp16 [M][K], 128-row boxes; B: fp16 [N][K], BN/PAIR-row boxes; kRowBytes
     // (128, or 64 / 32 for narrow K) of K per box, swizzled to match.  D: fp16 [M][N],
     // stored in 32-row x EPI_COLS boxes.
@@ -73,16 +73,18 @@ gemm_status_t prepare(int64_t M, int64_t N, int64_t K, const void* A, const void
     p.C = C;
     p.D = D;
     p.err = err;
+    p.split = 1;
     return GEMM_OK;
 }
 
 template <class Cfg>
 gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
-                  cudaStream_t stream, int sms, int dev) {
+                  cudaStream_t stream, int sms, int dev, int split = 1) {
     CUtensorMap ta, tb, td, tc;
     Params p;
     const gemm_status_t st = prepare<Cfg>(M, N, K, A, B, C, D, dev, ta, tb, td, tc, p);
     if (st != GEMM_OK) return st;
+    p.split = split;
     if (launch_config<Cfg>(ta, tb, ta, tb, td, tc, p, sms, dev, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -99,11 +101,17 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
         if (K <= 32)
             return M > 128 ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                            : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
-        switch (dispatch::dense_choice(M, N, K, 64, sms)) {
+        int res256[dispatch::kMaxSplit + 1], res128[dispatch::kMaxSplit + 1];
+        if (split_capacity<CfgF16Acc32>(sms, dev, res256) != cudaSuccess ||
+            split_capacity<CfgF16N128>(sms, dev, res128) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        const dispatch::DensePlan plan = dispatch::dense_plan(M, N, K, 64, sms, res256, res128);
+        switch (plan.choice) {
             case dispatch::DENSE_PAIR_256: return run<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
             case dispatch::DENSE_SINGLE_64: return run<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);
-            case dispatch::DENSE_SINGLE_128: return run<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev);
-            default: return run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev);
+            case dispatch::DENSE_SINGLE_128:
+                return run<CfgF16N128>(M, N, K, A, B, C, D, stream, sms, dev, plan.split);
+            default: return run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev, plan.split);
         }
     }
     return dispatch::use_pairs(M, N, sms) ? run<CfgF16Acc16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
@@ -111,11 +119,12 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
 }
 
 // ---------------------------------------------------------------- no-allocation variant
-// Scratch of gemm_f16_noalloc: one fixed block per device, part of the loaded
-// module, so the call never allocates.  20 MiB holds the stream-K partials (128 x 128
-// single-CTA tiles: 64 KB per SM) and flags of a device with up to 319 SMs (a 152-SM
-// GB300 needs 9.5 MiB).  Every
-// call shares it: calls that overlap on the GPU would overwrite each other's
+// Scratch of gemm_f16_noalloc, which keeps the stream-K schedule (units split the
+// k-blocks of the last tiles and the finishing unit adds the others' fp32 partials
+// from global memory): one fixed block per device, part of the loaded module, so the
+// call never allocates.  20 MiB holds the partials (128 x 128 single-CTA tiles: 64 KB
+// per SM) and flags of a device with up to 319 SMs (a 152-SM GB300 needs 9.5 MiB).
+// Every call shares it: calls that overlap on the GPU would overwrite each other's
 // partials and flags.
 constexpr size_t kStaticScratchBytes = size_t(20) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
@@ -153,9 +162,23 @@ gemm_status_t run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const 
 
 }  // namespace
 
+// Looks up the fixed block on device `dev` (the current device).  Under lazy module
+// loading the lookup is what makes the driver load this module, and with it the
+// block, on that device: the C ABI does it on its first accepted call on each device,
+// so that the block is in place before the caller reserves the rest of the device's
+// memory or starts a stream capture.
+bool setup_fixed_scratch(int dev) { return static_scratch(dev) != nullptr; }
+
 gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
                                       void* D, cudaStream_t stream, int sms, int dev) {
-    // the same instance choice as gemm_f16 with fp32 accumulation and K > 32
+    // Narrow K as gemm_f16 (one k-block: these instances never split, so they need no
+    // scratch); otherwise the stream-K rule of dense_choice over the fixed block.
+    if (K <= 16)
+        return M > 128 ? run<CfgF16K16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                       : run<CfgF16K16>(M, N, K, A, B, C, D, stream, sms, dev);
+    if (K <= 32)
+        return M > 128 ? run<CfgF16K32Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+                       : run<CfgF16K32>(M, N, K, A, B, C, D, stream, sms, dev);
     switch (dispatch::dense_choice(M, N, K, 64, sms)) {
         case dispatch::DENSE_PAIR_256: return run_noalloc<CfgF16Acc32Pair>(M, N, K, A, B, C, D, stream, sms, dev);
         case dispatch::DENSE_SINGLE_64: return run_noalloc<CfgF16N64>(M, N, K, A, B, C, D, stream, sms, dev);

@@ -86,6 +86,9 @@ __host__ __device__ constexpr bool operands_16bit(int kind) {
 // MMAs without scale factors: kind::f16 (FP16, BF16) or kind::f8f6f4 (FP8).
 __host__ __device__ constexpr bool is_dense(int kind) { return kind != KIND_NVFP4 && kind != KIND_MXFP8; }
 
+// Largest cluster of the cluster split (the portable cluster size).
+constexpr int kMaxClusterSplit = 8;
+
 // Upper bound on any single pipeline wait; legitimate waits are microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // Bound on the waits of the abandon path (in-flight copies / MMAs).
@@ -94,35 +97,47 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 struct Params {
     int M, N, K;
     int num_m_blocks, num_n_blocks, num_k_blocks;
+    int raster_group;  // m blocks per raster group of the tile order (tile_coords)
     const void* C;  // [M][N] fp16 (FP16 kinds) or bf16 (block-scaled), or null
     void* D;        // [M][N], same type as C
     unsigned int* err;
-    // Stream-K schedule: the last sk_tiles tiles (in tile order) are split across
-    // all units, each taking an equal contiguous share of their (tile, k-block)
-    // sequence before its whole tiles.  A tile cut between units is finished by
-    // the unit holding its k-block 0 (that piece ends the unit's share); the later
-    // pieces, which begin the next units' shares, leave fp32 partial sums in `ws`
-    // and raise their flag.  The remaining tiles are dealt whole, round robin.
+    // Stream-K schedule (only with a caller-provided scratch block): the last
+    // sk_tiles tiles (in tile order) are split across all units, each taking an
+    // equal contiguous share of their (tile, k-block) sequence before its whole
+    // tiles.  A tile cut between units is finished by the unit holding its k-block
+    // 0 (that piece ends the unit's share); the later pieces, which begin the next
+    // units' shares, leave fp32 partial sums in `ws` and raise their flag.  The
+    // remaining tiles are dealt whole, round robin.
     int sk_tiles;          // 0: every tile whole
     long long sk_total;    // sk_tiles * num_k_blocks
     float* ws;             // partials: [unit][rank][epilogue warp][chunk][col/4][lane][4]
     unsigned int* flags;   // [unit][rank][epilogue warp]: 1 once that partial is written
-    // Block-scaled kinds with packed scales (Config::kPackedScales): SFA and SFB
-    // regrouped into contiguous blocks [row group][16-byte scale column][rows][16 bytes]
-    // (SFA: groups of 128 rows; SFB: groups of BN rows, one per tile; rows past the
-    // matrix are zero), so that one stage's scales of a row group arrive in one bulk
-    // copy instead of one strided 16-byte row at a time.
-    const uint8_t* sfa_packed;
-    const uint8_t* sfb_packed;
-    int sf_cols16;  // 16-byte scale columns per row (blocks per row group)
+    // Cluster split (1 = off): the `split` CTAs of a (split,1,1) cluster share one
+    // tile, CTA r of the cluster summing k-blocks [r*nkb/split, (r+1)*nkb/split).
+    // Each leaves its fp32 sums in its own shared memory; after a cluster barrier
+    // the CTAs add the cluster's partials through distributed shared memory (each
+    // CTA a share of the tile's 32-row chunks, the partials in rank order), add C,
+    // round once and store.  No global scratch is involved.
+    int split;
 };
 
-enum SegKind : int { SEG_FULL = 0, SEG_PARTIAL = 1, SEG_OWNER = 2 };
+// How the block-scaled kinds move their scale factors (Config::SF_MODE).
+//   SF_RING   a ring of SF_SLOTS scale slots of SF_W bytes per row (SF_KB k-blocks), freed
+//             by the scale writers once read; the writers wait for the stage's MMAs
+//             before storing into its TMEM scale columns.
+//   SF_STAGE  one 16-byte slot per stage, refilled once the stage's MMAs are done; the
+//             writers wait only for the slot.  In CTA pairs each CTA loads half of the
+//             tile's SFB rows and multicasts them to both CTAs.
+//   SF_COPY   as SF_STAGE, but the writers repack the slot in shared memory into base
+//             tiles and the MMA thread copies them into TMEM with tcgen05.cp.
+enum ScaleMode : int { SF_RING = 0, SF_STAGE = 1, SF_COPY = 2 };
+
+enum SegKind : int { SEG_FULL = 0, SEG_PARTIAL = 1, SEG_OWNER = 2, SEG_SPLIT = 3 };
 
 // The work of one unit as a sequence of segments: tile, k blocks [k0, k1), kind.
 struct SegIter {
     long long pos, end;  // remaining stream-K share of the split tiles' (tile, k) sequence
-    int tile;            // next whole tile
+    int tile;            // next whole tile (cluster split: the cluster's tile, -1 once taken)
 };
 
 __device__ __forceinline__ long long sk_share_begin(const Params& p, int unit, int units) {
@@ -130,15 +145,32 @@ __device__ __forceinline__ long long sk_share_begin(const Params& p, int unit, i
 }
 
 __device__ __forceinline__ void seg_begin(const Params& p, int unit, int units, SegIter& it) {
+    if (p.split > 1) {
+        // cluster split (one CTA per unit): CTA r of the cluster takes its k range
+        const int r = unit % p.split;
+        it.tile = unit / p.split;
+        it.pos = static_cast<long long>(p.num_k_blocks) * r / p.split;
+        it.end = static_cast<long long>(p.num_k_blocks) * (r + 1) / p.split;
+        return;
+    }
     it.pos = sk_share_begin(p, unit, units);
     it.end = sk_share_begin(p, unit + 1, units);
     it.tile = unit;
 }
 
-// SK = false compiles the whole-tile schedule alone.
-template <bool SK>
+// SK = false compiles the whole-tile schedule alone; SPLIT adds the cluster split.
+template <bool SK, bool SPLIT>
 __device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it, int& tile, int& k0, int& k1,
                                          int& kind) {
+    if (SPLIT && p.split > 1) {
+        if (it.tile < 0) return false;
+        tile = it.tile;
+        k0 = static_cast<int>(it.pos);
+        k1 = static_cast<int>(it.end);
+        kind = SEG_SPLIT;
+        it.tile = -1;
+        return true;
+    }
     const int nkb = p.num_k_blocks;
     const int whole_tiles = p.num_m_blocks * p.num_n_blocks - (SK ? p.sk_tiles : 0);
     if (SK && it.pos < it.end) {
@@ -161,7 +193,8 @@ __device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it
 }
 
 template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
-          int EPI_WARPS_ = 4, int ROW_BYTES_ = 128, bool REG_DRAIN_ = false>
+          int EPI_WARPS_ = 4, int ROW_BYTES_ = 128, bool REG_DRAIN_ = false, int SF_MODE_ = 0, int SF_W_ = 16,
+          int SF_SLOTS_ = 2>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
@@ -202,21 +235,13 @@ struct Config {
                   "register drain: two 64-column chunks per warp, one staging buffer");
     // Registers per thread of each warpgroup under kRegDrain (launched with 128):
     // issuers and MMA, epilogue, scale writers, epilogue.  They add up to 4 x 128.
-    static constexpr int kRegsIssue = 48, kRegsEpi = 184, kRegsWriter = 96;
+    static constexpr int kRegsIssue = 64, kRegsEpi = 184, kRegsWriter = 80;
     static_assert(kRegsIssue + kRegsWriter + 2 * kRegsEpi == 4 * 128, "register split adds up to the launch's");
     static_assert(PAIR == 1 || PAIR == 2, "one CTA or a CTA pair per MMA");
     static constexpr bool kBlockScaled = (KIND == KIND_NVFP4 || KIND == KIND_MXFP8);
-    // NVFP4 stages and MXFP8 CTA-pair stages read their scales from packed blocks
-    // (one bulk copy per row group: SFA 128 rows, SFB one tile's BN rows; an MXFP8
-    // block serves four stages).  The
-    // single-CTA MXFP8 instance, whose skinny problems would pay the regrouping pass
-    // on top of a short, memory-bound GEMM, keeps the TMA boxes.
-    static constexpr bool kPackedScales = KIND == KIND_NVFP4 || (KIND == KIND_MXFP8 && PAIR == 2);
-    static_assert(!kRegDrain || kPackedScales, "register drain: NVFP4 (one scale issuer warp)");
-    // warps 0-7 (A issuer, MMA, B issuer, SFA issuer, epilogue x4), 8-11 scale
-    // writers, 12 SFB issuer; with kRegDrain warp 3 issues both scale streams and
-    // warps 12-15 are the second epilogue set.
-    static constexpr int THREADS = kRegDrain ? 512 : (kBlockScaled ? 416 : 256);
+    // warps 0-7 (A issuer, MMA, B issuer, scale loader, epilogue x4), 8-11 scale
+    // writers; with kRegDrain warps 12-15 are the second epilogue set.
+    static constexpr int THREADS = kRegDrain ? 512 : (kBlockScaled ? 384 : 256);
     // Bytes of K per operand row and stage: 128 (the 128-byte swizzle), or 64 / 32 for
     // problems whose whole K is narrower ("数据布局及其记号", swizzle section: the same
     // hierarchy with 8 x 64-byte and 8 x 32-byte atoms).  32 bytes of K per MMA.
@@ -229,28 +254,50 @@ struct Config {
 
     static constexpr int A_BYTES = BM * kRowBytes;
     static constexpr int B_BYTES = BN_CTA * kRowBytes;
-    static constexpr int SFB_GROUPS = kBlockScaled ? (BN + 127) / 128 : 0;  // 128-row scale groups
     static constexpr int SFB_TCOLS = kBlockScaled ? BN / 32 : 0;             // TMEM columns of a tile's SFB
     static_assert(!kBlockScaled || BN % 32 == 0, "block-scaled tiles of whole 32-row scale columns");
-    static constexpr int SFA_BYTES = kBlockScaled ? BM * 16 : 0;
-    static constexpr int SFB_BYTES = SFB_GROUPS * 128 * 16;
+    // Scale ring (block-scaled): SF_SLOTS slots, each holding SF_W bytes of every scale
+    // row this CTA needs (its 128 SFA rows, the tile's BN SFB rows), i.e. the scales of
+    // SF_KB k-blocks (NVFP4: 16 bytes per k-block and row; MXFP8: 4).  One TMA box per
+    // matrix fills a slot, so the strided scale rows are fetched SF_W bytes at a time.
+    static constexpr int SF_W = kBlockScaled ? SF_W_ : 0;
+    static constexpr int SF_SLOTS = kBlockScaled ? SF_SLOTS_ : 0;
+    static constexpr int SF_KB = KIND == KIND_NVFP4 ? SF_W_ / 16 : SF_W_ / 4;
+    static constexpr int SF_KB_BYTES = KIND == KIND_NVFP4 ? 16 : 4;  // scale bytes per row and k-block
+    static_assert(!kBlockScaled || (SF_W_ % 16 == 0 && SF_W_ >= 16 && SF_SLOTS_ >= 1), "16-byte multiple scale boxes");
+    // Scale copies (SF_COPY): the pages' tcgen05.cp.32x128b.warpx4 path.  The writers
+    // repack the stage's slot in place into 32-lane x 16-byte base tiles (lane l = rows
+    // l, l+32, l+64, l+96 of a 128-row group, one word each) and the MMA thread copies
+    // the tiles into TMEM, replicated to the four lane partitions, before the stage's
+    // MMAs.  Otherwise the writers place the same tiles with tcgen05.st.
+    static constexpr int SF_MODE = SF_MODE_;
+    static constexpr bool kScaleCp = kBlockScaled && SF_MODE_ == SF_COPY;
+    static constexpr bool kStageSlots = kBlockScaled && SF_MODE_ != SF_RING;
+    static_assert(!kStageSlots || (SF_W_ == 16 && SF_SLOTS_ == STAGES_), "one 16-byte scale slot per stage");
+    // Stage slots in CTA pairs: each CTA loads half of the tile's SFB rows and multicasts
+    // them into both CTAs' slots (a slot is free in both CTAs once the stage's MMAs, which
+    // signal both CTAs, are done).
+    static constexpr bool kSfbMulticast = kStageSlots && PAIR_ == 2;
+    static constexpr int SFB_BOX_ROWS = kSfbMulticast ? BN_ / 2 : BN_;
+    static constexpr int SFA_BYTES = BM * SF_W;  // per slot
+    static constexpr int SFB_BYTES = BN * SF_W;
     static constexpr uint32_t TX_BYTES = PAIR * (A_BYTES + B_BYTES);             // both CTAs' operands
-    static constexpr uint32_t SF_TX_BYTES = kBlockScaled ? (BM + BN) * 16 : 0;  // this CTA's scales
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;  // 1024-byte aligned
+    static constexpr int OFF_SFB = OFF_SFA + SF_SLOTS * SFA_BYTES;
+    static constexpr int OFF_EPI = OFF_SFB + SF_SLOTS * SFB_BYTES;  // 1024-byte aligned
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-    // barriers: full[S], empty[S], sf_full[S], tmem_full[ACC], tmem_empty[ACC], drain,
+    // barriers: full[S], empty[S], sf_full[R], sf_empty[R], tmem_full[ACC], tmem_empty[ACC], drain,
     // c_load[EPI_WARPS][EPI_BUFS]
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = STAGES;
-    static constexpr int BAR_SFFULL = 2 * STAGES;
-    static constexpr int BAR_TFULL = 3 * STAGES;
-    static constexpr int BAR_TEMPTY = 3 * STAGES + ACC_BUFS;
-    static constexpr int BAR_DRAIN = 3 * STAGES + 2 * ACC_BUFS;
+    static constexpr int BAR_SFFULL = 2 * STAGES;                // [scale slot]: boxes landed
+    static constexpr int BAR_SFEMPTY = BAR_SFFULL + SF_SLOTS;     // [scale slot]: writers done with it
+    static constexpr int BAR_TFULL = BAR_SFEMPTY + SF_SLOTS;
+    static constexpr int BAR_TEMPTY = BAR_TFULL + ACC_BUFS;
+    static constexpr int BAR_DRAIN = BAR_TEMPTY + ACC_BUFS;
     static constexpr int BAR_CLOAD = BAR_DRAIN + 1;  // [epilogue warp][staging buffer]: C chunk landed
     static constexpr int NUM_BARS = BAR_CLOAD + EPI_WARPS * EPI_BUFS;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // TMEM base address, abort flag
@@ -273,16 +320,25 @@ struct Config {
     static_assert(BN % (16 * PAIR) == 0 && BN >= 16 && BN <= 256, "MMA N: multiple of 16 (32 for a pair), <= 256");
     static_assert(B_BYTES % 1024 == 0, "B stages stay 1024-byte aligned");
     static_assert(OFF_EPI % 1024 == 0, "staging buffers start on a swizzle-atom boundary");
+    // Cluster split (Params::split > 1): single CTAs, 4 epilogue warps, fp32
+    // accumulation, 128-byte operand rows.  After the mainloop the operand stages are
+    // idle and hold the CTA's fp32 partial tile, [quarter][chunk][col/4][lane][4].
+    // Each CTA receives, in its idle operand stages, one fp32 slot of 32 rows x EPI_COLS
+    // per (owned chunk, source CTA): at most (4 * BN / EPI_COLS + kMaxClusterSplit - 1) slots.
+    static constexpr bool kSplit = PAIR == 1 && EPI_WARPS_ == 4 && KIND_ != KIND_F16_ACC16 && ROW_BYTES_ == 128;
+    static_assert(!kSplit || (4 * BN / EPI_COLS + kMaxClusterSplit - 1) * 32 * EPI_COLS * 4 <= STAGES * (A_BYTES + B_BYTES),
+                  "the pushed partials fit the operand stages");
 };
 
-// Output tile -> (m block, n block), grouping 8 m blocks so that concurrently
-// running tiles share A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-    constexpr int G = 8;
-    const int per_group = G * num_n;
+// Output tile -> (m block, n block).  Tiles run down groups of `group` m blocks
+// (column by column within a group), so that the tiles in flight at one time share
+// a few A panels and B panels in L2; the host picks the group so that one wave's
+// panels fit in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group, int& mb, int& nb) {
+    const int per_group = group * num_n;
     const int g = tile / per_group;
-    const int first_m = g * G;
-    const int gs = min(num_m - first_m, G);
+    const int first_m = g * group;
+    const int gs = min(num_m - first_m, group);
     const int r = tile - g * per_group;
     mb = first_m + r % gs;
     nb = r / gs;
@@ -403,26 +459,25 @@ __device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int
     }
 }
 
-// Scale-factor writer for one TMEM lane quarter.  The stage's scale boxes sit in
-// shared memory row-major: row r of a box at bytes 16r .. 16r+15 holds scale
-// blocks sfk = 16c .. 16c+15 of that row.  Lane l of the warp (TMEM lane
-// 32q + l) receives, for each copy set j, the base-tile row l: SFA scales of rows
-// l, l+32, l+64, l+96 in columns 0..3 (TCol = m // 32, the four scales of the
-// MMA in bytes 0..3, byte = sfk), then the SFB scales of rows l + 32c in
-// columns 4 + c ("数据布局及其记号", block-scaled section).  NVFP4 has one copy
-// set per MMA (word j of each row = that MMA's 4 scales); MXFP8 has one copy set
-// per stage (word `word` of each row = the stage's 4 scales, one per MMA, picked
-// by the MMA's scale-factor ID).  Every quarter writes the same values: together
-// the four warps replicate the tile to the four lane partitions.
-template <int KIND, int SFB_TCOLS>
-__device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t* raw_b, int lane, int word,
-                                             uint32_t taddr) {
+// Scale-factor writer for one TMEM lane quarter.  The k-block's scales sit in a scale
+// slot row-major: row r at raw + r * ROW holds the SF_KB_BYTES scale bytes of that row
+// for this k-block (NVFP4: 16 = four per MMA; MXFP8: 4 = one per MMA).  Lane l of the
+// warp (TMEM lane 32q + l) receives, for each copy set j, the base-tile row l: SFA
+// scales of rows l, l+32, l+64, l+96 in columns 0..3 (TCol = m // 32, the four scales
+// of the MMA in bytes 0..3, byte = sfk), then the SFB scales of rows l + 32c in columns
+// 4 + c ("数据布局及其记号", block-scaled section).  NVFP4 has one copy set per MMA (word
+// j of each row = that MMA's 4 scales); MXFP8 has one copy set per stage (each row's
+// word = the stage's 4 scales, one per MMA, picked by the MMA's scale-factor ID).  Every
+// quarter writes the same values: together the four warps replicate the tile to the
+// four lane partitions.
+template <int KIND, int SFB_TCOLS, int ROW>
+__device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t* raw_b, int lane, uint32_t taddr) {
     constexpr int SET = 4 + SFB_TCOLS;  // SFA columns (128 rows) + SFB columns (BN rows)
     if constexpr (KIND == KIND_NVFP4) {
         uint32_t R[SET][4];
 #pragma unroll
         for (int c = 0; c < SET; ++c) {
-            const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * 16 : raw_b + layout::sf_row(lane, c - 4) * 16;
+            const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * ROW : raw_b + layout::sf_row(lane, c - 4) * ROW;
             const uint4 x = *reinterpret_cast<const uint4*>(src);
             R[c][0] = x.x;
             R[c][1] = x.y;
@@ -442,8 +497,8 @@ __device__ __forceinline__ void write_scales(const uint8_t* raw_a, const uint8_t
         uint32_t out[SET];
 #pragma unroll
         for (int c = 0; c < SET; ++c) {
-            const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * 16 : raw_b + layout::sf_row(lane, c - 4) * 16;
-            out[c] = reinterpret_cast<const uint32_t*>(src)[word];
+            const uint8_t* src = (c < 4) ? raw_a + layout::sf_row(lane, c) * ROW : raw_b + layout::sf_row(lane, c - 4) * ROW;
+            out[c] = *reinterpret_cast<const uint32_t*>(src);
         }
         tmem_st_32x32b_x8(taddr, *reinterpret_cast<const uint32_t(*)[8]>(&out[0]));
         if constexpr (SET == 12) tmem_st_32x32b_x4(taddr + 8, *reinterpret_cast<const uint32_t(*)[4]>(&out[8]));
@@ -514,7 +569,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // the leader's A and B issuers, and (block-scaled) every scale-writer warp
             mbar_init(bar(Cfg::BAR_FULL + s), 2 + (kBS ? 4 * PAIR : 0));
             mbar_init(bar(Cfg::BAR_EMPTY + s), 1);
-            mbar_init(bar(Cfg::BAR_SFFULL + s), 2);  // SFA and SFB issuers
+        }
+        for (int r = 0; r < Cfg::SF_SLOTS; ++r) {
+            mbar_init(bar(Cfg::BAR_SFFULL + r), 1);   // the scale loader (SFA and SFB boxes)
+            mbar_init(bar(Cfg::BAR_SFEMPTY + r), 4);  // the four scale-writer warps
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             mbar_init(bar(Cfg::BAR_TFULL + b), 1);
@@ -530,7 +588,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
         if (p.C != nullptr) tma_prefetch_desc(&tmC);
-        if constexpr (kBS && !Cfg::kPackedScales) {
+        if constexpr (kBS) {
             tma_prefetch_desc(&tmSFA);
             tma_prefetch_desc(&tmSFB);
         }
@@ -559,8 +617,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     griddep_launch_dependents();
 
     // ------------------------------------------------------------------ TMA issuers
-    // role 0: A, 1: B, 2: SFA, 3: SFB.  Each waits for its stage slot to be released
-    // by the MMAs that last read it, arms its barrier with its bytes and issues one box.
+    // role 0: A, 1: B.  Each waits for its stage slot to be released by the MMAs that
+    // last read it, arms the leader's `full` barrier with its bytes and issues one box.
     auto issue_loop = [&](const int role) {
         int s = 0;
         uint32_t ph = 0;
@@ -572,12 +630,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         seg_begin(p, cluster, num_clusters, it);
         int tile, k0, k1, kind;
         bool first_seg = true;
-        while (ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind)) {
+        while (ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
             int mb, nb;
-            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
+            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
             const int m0 = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM;  // this CTA's A rows
-            const int nb0 = nb * BN;                                              // tile's first column
-            const int n0 = nb0 + static_cast<int>(rank) * Cfg::BN_CTA;           // this CTA's B rows
+            const int n0 = nb * BN + static_cast<int>(rank) * Cfg::BN_CTA;        // this CTA's B rows
             for (int kb = k0; kb < k1; ++kb) {
                 if (!wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err)) {
                     ok = false;
@@ -595,48 +652,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     continue;
                 }
 #endif
-                if (role <= 1) {
-                    const int kx = kb * Cfg::kKCoordPerStage;
-                    const uint32_t dst = role == 0 ? sbase + Cfg::OFF_A + s * Cfg::A_BYTES
-                                                   : sbase + Cfg::OFF_B + s * Cfg::B_BYTES;
-                    const CUtensorMap* map = role == 0 ? &tmA : &tmB;
-                    const int y = role == 0 ? m0 : n0;
-                    const uint32_t bytes = PAIR * (role == 0 ? Cfg::A_BYTES : Cfg::B_BYTES);
-                    if constexpr (kPair) {
-                        if (leader) mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
-                        tma_load_2d_pair(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y);
-                    } else {
-                        mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
-                        tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
-                    }
-                } else if constexpr (kBS) {
-                    // 16 scale bytes per row per box; NVFP4 uses all 16 in this stage,
-                    // MXFP8 uses 4 of them (so the same box serves 4 stages).
-                    const int sfx = (KIND == KIND_NVFP4) ? kb * 16 : (kb >> 2) * 16;
-                    const uint32_t sb = bar(Cfg::BAR_SFFULL + s);
-                    if constexpr (Cfg::kPackedScales) {
-                        // block (row group, 16-byte column): the same bytes the box holds
-                        const size_t cols = static_cast<size_t>(p.sf_cols16);
-                        const int sfc = KIND == KIND_NVFP4 ? kb : (kb >> 2);  // MXFP8: 4 stages per column
-                        if (role == 2) {
-                            mbar_arrive_expect_tx(sb, Cfg::BM * 16);
-                            bulk_load(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES,
-                                      p.sfa_packed + ((m0 >> 7) * cols + sfc) * 2048, 2048, sb);
-                        }
-                        if (role == 3 || Cfg::kRegDrain) {  // kRegDrain: one warp issues both
-                            // SFB blocks hold a whole tile's BN rows
-                            constexpr uint32_t kSfbBlock = BN * 16;
-                            mbar_arrive_expect_tx(sb, kSfbBlock);
-                            bulk_load(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES,
-                                      p.sfb_packed + (static_cast<size_t>(nb) * cols + sfc) * kSfbBlock, kSfbBlock, sb);
-                        }
-                    } else if (role == 2) {
-                        mbar_arrive_expect_tx(sb, Cfg::BM * 16);
-                        tma_load_2d(sbase + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, &tmSFA, sb, sfx, m0);
-                    } else {
-                        mbar_arrive_expect_tx(sb, BN * 16);
-                        tma_load_2d(sbase + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, &tmSFB, sb, sfx, nb0);
-                    }
+                const int kx = kb * Cfg::kKCoordPerStage;
+                const uint32_t dst =
+                    role == 0 ? sbase + Cfg::OFF_A + s * Cfg::A_BYTES : sbase + Cfg::OFF_B + s * Cfg::B_BYTES;
+                const CUtensorMap* map = role == 0 ? &tmA : &tmB;
+                const int y = role == 0 ? m0 : n0;
+                const uint32_t bytes = PAIR * (role == 0 ? Cfg::A_BYTES : Cfg::B_BYTES);
+                if constexpr (kPair) {
+                    if (leader) mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
+                    tma_load_2d_pair(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y);
+                } else {
+                    mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
+                    tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
                 }
                 ++loads[s];
                 if (++s == STAGES) {
@@ -647,6 +674,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             first_seg = false;
         }
         (void)kind;
+        (void)first_seg;
         if (ok && role == 0) {
             // Wait until the MMAs have released every stage, so that no
             // tcgen05.commit arrival is still in flight when the CTA exits.
@@ -662,13 +690,71 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // Abandoning: let every issued TMA copy land before the CTA exits.
             for (int i = 0; i < STAGES; ++i) {
                 if (loads[i] == 0) continue;
-                if (role >= 2)
-                    wait_bar_drain(bar(Cfg::BAR_SFFULL + i), (loads[i] - 1u) & 1u);
-                else if (!kPair || leader)
-                    wait_bar_drain(bar(Cfg::BAR_FULL + i), (loads[i] - 1u) & 1u);
+                if (!kPair || leader) wait_bar_drain(bar(Cfg::BAR_FULL + i), (loads[i] - 1u) & 1u);
             }
             // the peer's operand copies signal the leader's barriers: give them time
-            if (kPair && role <= 1) pause_ns(kDrainLimitNs / 4);
+            if (kPair) pause_ns(kDrainLimitNs / 4);
+        }
+    };
+
+    // ------------------------------------------------------------------ scale loader
+    // (block-scaled only) Lane 0 of one warp.  A segment's k-blocks fall into groups of
+    // SF_KB (the absolute k-block / SF_KB); for each group the segment touches, one
+    // scale slot is filled with a TMA box of the caller's row-major SFA (SF_W bytes x
+    // this CTA's 128 rows) and one of SFB (SF_W bytes x the tile's BN rows), unswizzled;
+    // rows past M or N and bytes past the row end read as zero.  A slot is refilled
+    // once the four scale writers have read it.
+    auto scale_loop = [&]() {
+        if constexpr (kBS) {
+            constexpr int R = Cfg::SF_SLOTS;
+            int r = 0;
+            uint32_t ph = 0;
+            uint32_t loads[R];
+#pragma unroll
+            for (int i = 0; i < R; ++i) loads[i] = 0;
+            bool ok = true;
+            SegIter it;
+            seg_begin(p, cluster, num_clusters, it);
+            int tile, k0, k1, kind;
+            while (ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
+                int mb, nb;
+                tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
+                const int m0 = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM;  // this CTA's SFA rows
+                const int nb0 = nb * BN;                                              // the tile's SFB rows
+                // stage slots: slot r = stage, refilled once the stage's MMAs are done, with
+                // the 16-byte box of k-block kb (MXFP8: the box holding it); ring: one box
+                // per group of SF_KB k-blocks the segment touches
+                const int g_end = Cfg::kStageSlots ? k1 : (k1 + Cfg::SF_KB - 1) / Cfg::SF_KB;
+                for (int g = Cfg::kStageSlots ? k0 : k0 / Cfg::SF_KB; g < g_end; ++g) {
+                    const uint32_t free_bar = Cfg::kStageSlots ? bar(Cfg::BAR_EMPTY + r) : bar(Cfg::BAR_SFEMPTY + r);
+                    if (!wait_bar(free_bar, ph ^ 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const int x = Cfg::kStageSlots ? (KIND == KIND_NVFP4 ? g : (g >> 2)) * 16 : g * Cfg::SF_W;
+                    const uint32_t sb = bar(Cfg::BAR_SFFULL + r);
+                    mbar_arrive_expect_tx(sb, (Cfg::BM + BN) * Cfg::SF_W);  // all that lands in this CTA
+                    tma_load_2d(sbase + Cfg::OFF_SFA + r * Cfg::SFA_BYTES, &tmSFA, sb, x, m0);
+                    if constexpr (Cfg::kSfbMulticast) {
+                        const int half = static_cast<int>(rank) * Cfg::SFB_BOX_ROWS;  // this CTA's half of SFB
+                        tma_load_2d_multicast(sbase + Cfg::OFF_SFB + r * Cfg::SFB_BYTES + half * Cfg::SF_W, &tmSFB, sb, x,
+                                              nb0 + half, 0x3);
+                    } else {
+                        tma_load_2d(sbase + Cfg::OFF_SFB + r * Cfg::SFB_BYTES, &tmSFB, sb, x, nb0);
+                    }
+                    ++loads[r];
+                    if (++r == R) {
+                        r = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            (void)kind;
+            if (!ok) {
+                // Abandoning: let every issued scale box land before the CTA exits.
+                for (int i = 0; i < R; ++i)
+                    if (loads[i] != 0) wait_bar_drain(bar(Cfg::BAR_SFFULL + i), (loads[i] - 1u) & 1u);
+            }
         }
     };
 
@@ -683,13 +769,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // descriptor of stage 0; stage s adds s * (bytes / 16) to the start address
             const uint64_t adesc0 = layout::umma_smem_desc_kmajor(sbase + Cfg::OFF_A, Cfg::kRowBytes);
             const uint64_t bdesc0 = layout::umma_smem_desc_kmajor(sbase + Cfg::OFF_B, Cfg::kRowBytes);
+            // scale tiles (copy mode): 32 rows x 16 bytes, row after row; +32 per 512-byte tile
+            const uint64_t sfa_desc0 = layout::umma_smem_desc_noswizzle(sbase + Cfg::OFF_SFA, 128, 128);
+            const uint64_t sfb_desc0 = layout::umma_smem_desc_noswizzle(sbase + Cfg::OFF_SFB, 128, 128);
+            // copy mode: stage st's base tiles into its TMEM scale columns, replicated to the
+            // four lane partitions (SFA to TCol 0-3 of each copy set, the 128-row group h of
+            // SFB to TCol 4 + 4h)
+            auto issue_scale_copies = [&](int st) {
+                if constexpr (Cfg::kScaleCp) {
+                    const uint32_t sf_t = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + st * Cfg::SF_COLS_PER_STAGE);
+                    const uint64_t da = sfa_desc0 + static_cast<uint64_t>((st * Cfg::SFA_BYTES) >> 4);
+                    const uint64_t db = sfb_desc0 + static_cast<uint64_t>((st * Cfg::SFB_BYTES) >> 4);
+                    constexpr int SETS = KIND == KIND_NVFP4 ? 4 : 1;
+#pragma unroll
+                    for (int j = 0; j < SETS; ++j) {
+                        const uint32_t t = sf_t + j * Cfg::SF_COLS_PER_COPYSET;
+                        if constexpr (kPair) {
+                            tc_cp_32x128b_warpx4_pair(t, da + 32 * j);
+#pragma unroll
+                            for (int h = 0; h < BN / 128; ++h) tc_cp_32x128b_warpx4_pair(t + 4 + 4 * h, db + 128 * h + 32 * j);
+                        } else {
+                            tc_cp_32x128b_warpx4(t, da + 32 * j);
+#pragma unroll
+                            for (int h = 0; h < BN / 128; ++h) tc_cp_32x128b_warpx4(t + 4 + 4 * h, db + 128 * h + 32 * j);
+                        }
+                    }
+                }
+            };
+            bool cp_ahead = false;  // the current stage's scale copies were issued one stage early
             bool ok = true;
             int s = 0;
             uint32_t ph = 0;
             SegIter it;
             seg_begin(p, cluster, num_clusters, it);
             int tile, k0, k1, kind;
-            for (int t_local = 0; ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind); ++t_local) {
+            for (int t_local = 0; ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind); ++t_local) {
                 const int buf = (ACC_BUFS == 1) ? 0 : (t_local & 1);
                 const uint32_t use = static_cast<uint32_t>(ACC_BUFS == 1 ? t_local : (t_local >> 1));
                 if (!wait_bar<kPair>(bar(Cfg::BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag, p.err)) {
@@ -732,6 +846,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                     } else {
                         const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE);
+                        if constexpr (Cfg::kScaleCp) {
+                            if (!cp_ahead) issue_scale_copies(s);
+                            cp_ahead = false;
+                        }
                         if constexpr (KIND == KIND_NVFP4) {
                             constexpr uint32_t idesc = idesc_block_scaled(kM, BN, 1u, false, 0u);
 #pragma unroll
@@ -754,6 +872,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                     mma_mxf8f6f4_1x(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
                                                     acc_kb || j != 0);
                             }
+                        }
+                    }
+                    if constexpr (Cfg::kScaleCp) {
+                        // the next stage's scale copies now, if its data is already there: they
+                        // then land while this stage's MMAs run
+                        const int sn = s + 1 == STAGES ? 0 : s + 1;
+                        const uint32_t pn = s + 1 == STAGES ? ph ^ 1u : ph;
+                        if (kPair ? mbar_test_wait_cluster(bar(Cfg::BAR_FULL + sn), pn)
+                                  : mbar_try_wait(bar(Cfg::BAR_FULL + sn), pn)) {
+                            tc_fence_after_sync();
+                            issue_scale_copies(sn);
+                            cp_ahead = true;
                         }
                     }
                     if constexpr (kPair)
@@ -787,21 +917,110 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     auto writer_role = [&]() {
         if constexpr (kBS) {
             // -------------------------------------------------------------- scale writers
+            // Per k-block: the scales from the scale slot (waited for at the slot's first
+            // k-block of the segment, released to the loader after its last), into the
+            // stage's TMEM scale columns once the MMAs that last read those columns have
+            // completed; then arrive on the stage's `full` barrier.
             const int q = warp & 3;  // TMEM lane quarter this warp may access
             const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, r = 0;
+            uint32_t ph = 0, rph = 0;
             bool ok = true;
             SegIter it;
             seg_begin(p, cluster, num_clusters, it);
             int tile, k0, k1, kind;
-            while (ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind)) {
+            while (ok && Cfg::kScaleCp && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
+                // copy mode: warp q repacks 128-row group q of the stage's slot in place
+                // (group 0: SFA, groups 1 ..: SFB rows 128(q-1) ..) into the base tiles
+                // the MMA thread copies: NVFP4 one tile per MMA j (word j of each row),
+                // MXFP8 one tile (the stage's word, kb % 4).
+                constexpr int GROUPS = 1 + BN / 128;
+                uint8_t* grp = q == 0 ? smem + Cfg::OFF_SFA : smem + Cfg::OFF_SFB + (q - 1) * 2048;
                 for (int kb = k0; kb < k1; ++kb) {
                     ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_SFFULL + s), ph, abort_flag, p.err));
                     if (!ok) break;
-                    write_scales<KIND, Cfg::SFB_TCOLS>(
-                        smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES, smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES, lane,
-                        kb & 3, lane_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE));
+                    if (q < GROUPS) {
+                        uint8_t* g = grp + s * (q == 0 ? Cfg::SFA_BYTES : Cfg::SFB_BYTES);
+                        uint4 x[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) x[i] = *reinterpret_cast<const uint4*>(g + (lane + 32 * i) * 16);
+                        __syncwarp();
+                        auto word = [](const uint4& v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; };
+                        if constexpr (KIND == KIND_NVFP4) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                *reinterpret_cast<uint4*>(g + 512 * j + 16 * lane) =
+                                    make_uint4(word(x[0], j), word(x[1], j), word(x[2], j), word(x[3], j));
+                        } else {
+                            const int j = kb & 3;
+                            *reinterpret_cast<uint4*>(g + 16 * lane) =
+                                make_uint4(word(x[0], j), word(x[1], j), word(x[2], j), word(x[3], j));
+                        }
+                        fence_proxy_async_smem();  // the tiles are read by tcgen05.cp (async proxy)
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (kPair)
+                            mbar_arrive_cluster(leader_bar(Cfg::BAR_FULL + s));  // release: shared-memory data
+                        else
+                            mbar_arrive(bar(Cfg::BAR_FULL + s));
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            while (ok && Cfg::SF_MODE == SF_STAGE &&
+                   seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
+                // stage slots: the slot's load was issued after the stage's previous MMAs
+                // completed, so one wait covers both the data and the TMEM columns
+                for (int kb = k0; kb < k1; ++kb) {
+                    ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_SFFULL + s), ph, abort_flag, p.err));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const int off = KIND == KIND_NVFP4 ? 0 : (kb & 3) * Cfg::SF_KB_BYTES;
+                    write_scales<KIND, Cfg::SFB_TCOLS, Cfg::SF_W>(
+                        smem + Cfg::OFF_SFA + s * Cfg::SFA_BYTES + off, smem + Cfg::OFF_SFB + s * Cfg::SFB_BYTES + off,
+                        lane, lane_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE));
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (kPair)
+                            mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_FULL + s));
+                        else
+                            mbar_arrive(bar(Cfg::BAR_FULL + s));
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            while (ok && Cfg::SF_MODE == SF_RING &&
+                   seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
+                for (int kb = k0; kb < k1; ++kb) {
+                    const int in_slot = kb % Cfg::SF_KB;
+                    if (kb == k0 || in_slot == 0) {
+                        ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_SFFULL + r), rph, abort_flag, p.err));
+                        if (!ok) break;
+                    }
+                    ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_EMPTY + s), ph ^ 1u, abort_flag, p.err));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const int off = in_slot * Cfg::SF_KB_BYTES;
+                    write_scales<KIND, Cfg::SFB_TCOLS, Cfg::SF_W>(
+                        smem + Cfg::OFF_SFA + r * Cfg::SFA_BYTES + off, smem + Cfg::OFF_SFB + r * Cfg::SFB_BYTES + off,
+                        lane, lane_base + static_cast<uint32_t>(Cfg::SF_COL0 + s * Cfg::SF_COLS_PER_STAGE));
+                    if (kb == k1 - 1 || in_slot == Cfg::SF_KB - 1) {
+                        __syncwarp();  // every lane has read the slot
+                        if (lane == 0) mbar_arrive(bar(Cfg::BAR_SFEMPTY + r));
+                        if (++r == Cfg::SF_SLOTS) {
+                            r = 0;
+                            rph ^= 1u;
+                        }
+                    }
                     tmem_st_wait();
                     tc_fence_before_sync();
                     __syncwarp();
@@ -817,7 +1036,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         s = 0;
                         ph ^= 1u;
                     }
-
                 }
             }
         }
@@ -850,16 +1068,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         SegIter it;
         seg_begin(p, cluster, num_clusters, it);
         int tile, k0, k1, kind;
-        for (; ok && seg_next<Cfg::kStreamK>(p, num_clusters, it, tile, k0, k1, kind); ++t_local) {
+        for (; ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind); ++t_local) {
             const int buf = (ACC_BUFS == 1) ? 0 : (t_local % ACC_BUFS);
             const uint32_t use = static_cast<uint32_t>(t_local / ACC_BUFS);
             int mb, nb;
-            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, mb, nb);
+            tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
             // first output row of this warp
             const int m_warp = mb * Cfg::BM_TILE + static_cast<int>(rank) * Cfg::BM + q * 32;
             const int n0 = nb * BN;
             const bool rows_in = m_warp < p.M;
-            (void)k0;
+            if constexpr (Cfg::kSplit) {
+                if (kind == SEG_SPLIT) {
+                    // Cluster split: the accumulator is pushed to the tile's owners after the
+                    // roles (split_push), once every CTA of the cluster is past its mainloop.
+                    ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
+                    if (!ok) break;
+                    continue;
+                }
+            }
             if (kSK && kind == SEG_PARTIAL) {
                 // A later piece of a tile another unit finishes: publish the fp32 sums.
                 ok = __all_sync(0xffffffffu, wait_bar(bar(Cfg::BAR_TFULL + buf), use & 1u, abort_flag, p.err));
@@ -884,7 +1110,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (kPair)
-                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                        mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_TEMPTY + buf));
                     else
                         mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
                     st_release_gpu(partial_flag<Cfg>(p, cluster, rank, e), 1u);
@@ -972,7 +1198,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (kPair)
-                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                        mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_TEMPTY + buf));
                     else
                         mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
                 }
@@ -1000,7 +1226,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (kPair)
-                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                        mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_TEMPTY + buf));
                     else
                         mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
                 }
@@ -1079,7 +1305,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (kPair)
-                        mbar_arrive_cluster(leader_bar(Cfg::BAR_TEMPTY + buf));
+                        mbar_arrive_cluster_relaxed(leader_bar(Cfg::BAR_TEMPTY + buf));
                     else
                         mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
                 }
@@ -1093,6 +1319,120 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         __syncwarp();
     };
+    // Cluster split.  The tile's 32-row x EPI_COLS chunks u = 4g + q (q: lane quarter, g:
+    // column chunk) are owned by the cluster's CTAs in turn: chunk u by CTA u % S (S =
+    // cluster size), its (u / S)-th.  Each CTA owns at most ceil(UNITS / S) chunks and
+    // keeps, in its idle operand stages, one fp32 slot per (owned chunk, source CTA):
+    // slot (k, s) at k * S + s, [col/4][lane][4] inside.
+    constexpr int UNIT_BYTES = 32 * Cfg::EPI_COLS * 4;
+    // split_push (after every CTA of the cluster is past its mainloop): epilogue warp q
+    // reads its lane quarter of the accumulator chunk by chunk and stores each chunk into
+    // the owner's slot for this CTA through distributed shared memory.
+    auto split_push = [&]() {
+        if constexpr (Cfg::kSplit) {
+            constexpr int EC = Cfg::EPI_COLS;
+            const int q = warp & 3;
+            const int S = p.split;
+            const int r = static_cast<int>(blockIdx.x) % S;
+            const int nkb = p.num_k_blocks;
+            const bool none = nkb * r / S == nkb * (r + 1) / S;  // an empty k range contributes zeros
+            tc_fence_after_sync();
+            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int g = 0; g < BN / EC; ++g) {
+                const int u = 4 * g + q;
+                const int owner = u % S, k = u / S;
+                uint32_t v[EC];
+                load_chunk<EC>(tacc, g * EC, v);
+                tmem_ld_wait();
+                const uint32_t dst = mapa_shared(
+                    sbase + Cfg::OFF_A + static_cast<uint32_t>((k * S + r) * UNIT_BYTES + lane * 16),
+                    static_cast<uint32_t>(owner));
+#pragma unroll
+                for (int i = 0; i < EC / 4; ++i) {
+                    if (none)
+                        st_shared_cluster_u4(dst + i * 512, 0u, 0u, 0u, 0u);
+                    else
+                        st_shared_cluster_u4(dst + i * 512, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+            }
+        }
+    };
+    // split_reduce (after every slot has landed): the CTA's owned chunks are dealt to its
+    // epilogue warps; each adds the chunk's S slots in rank order, adds C, rounds once,
+    // stages and stores.
+    auto split_reduce = [&]() {
+        if constexpr (Cfg::kSplit) {
+            constexpr int EC = Cfg::EPI_COLS;
+            constexpr int EB = Cfg::EPI_BUFS;
+            constexpr int UNITS = 4 * (BN / EC);
+            const int e = warp - 4;
+            const int S = p.split;
+            const int r = static_cast<int>(blockIdx.x) % S;
+            int mb, nb;
+            tile_coords(static_cast<int>(blockIdx.x) / S, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
+            uint8_t* stg = smem + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
+            const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
+            const bool has_c = p.C != nullptr;
+            uint32_t cph = 0, cpending = 0;
+            bool ok = *abort_flag == 0;
+            int j = 0;
+            for (int k = e, u = r + e * S; ok && u < UNITS; k += 4, u += 4 * S) {
+                const int q = u & 3, g = u >> 2;
+                const int m_warp = mb * Cfg::BM + q * 32;
+                const int nc = nb * BN + g * EC;
+                if (m_warp >= p.M || nc >= p.N) continue;  // warp-uniform
+                const int b = j % EB;
+                ++j;
+                const uint32_t cb = bar(Cfg::BAR_CLOAD + e * EB + b);
+                if (lane == 0) {
+                    bulk_wait_group_read<EB - 1>();  // buffer b's previous store has read it
+                    if (has_c) {
+                        mbar_arrive_expect_tx(cb, Cfg::EPI_BUF_BYTES);
+                        tma_load_2d(stg_u32 + b * Cfg::EPI_BUF_BYTES, &tmC, cb, nc, m_warp);
+                    }
+                }
+                if (has_c) cpending |= 1u << b;
+                __syncwarp();
+                uint32_t acc[EC];
+#pragma unroll
+                for (int i = 0; i < EC; ++i) acc[i] = 0u;  // +0.0f
+                const float4* slot = reinterpret_cast<const float4*>(smem + Cfg::OFF_A + k * S * UNIT_BYTES) + lane;
+                for (int src = 0; src < S; ++src, slot += UNIT_BYTES / 16) {
+#pragma unroll
+                    for (int i = 0; i < EC / 4; ++i) {
+                        const float4 v = slot[i * 32];
+                        acc[4 * i] = __float_as_uint(__uint_as_float(acc[4 * i]) + v.x);
+                        acc[4 * i + 1] = __float_as_uint(__uint_as_float(acc[4 * i + 1]) + v.y);
+                        acc[4 * i + 2] = __float_as_uint(__uint_as_float(acc[4 * i + 2]) + v.z);
+                        acc[4 * i + 3] = __float_as_uint(__uint_as_float(acc[4 * i + 3]) + v.w);
+                    }
+                }
+                if (has_c) {
+                    ok = __all_sync(0xffffffffu, wait_bar(cb, (cph >> b) & 1u, abort_flag, p.err));
+                    cph ^= 1u << b;
+                    cpending &= ~(1u << b);
+                    if (!ok) break;
+                    stage_chunk<KIND, EC, true>(acc, stg + b * Cfg::EPI_BUF_BYTES, lane);
+                } else {
+                    stage_chunk<KIND, EC, false>(acc, stg + b * Cfg::EPI_BUF_BYTES, lane);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, nc, m_warp);
+                    bulk_commit_group();
+                }
+            }
+            if (lane == 0) {
+                for (int b = 0; b < EB; ++b)
+                    if (cpending & (1u << b)) wait_bar_drain(bar(Cfg::BAR_CLOAD + e * EB + b), (cph >> b) & 1u);
+                bulk_wait_group_all();
+            }
+            __syncwarp();
+        }
+    };
+
     if constexpr (Cfg::kRegDrain) {
         // Each warpgroup sets its register budget inside its own branch (all four
         // warps execute the same setmaxnreg, and the code after it is compiled to
@@ -1104,7 +1444,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (warp == 1)
                 mma_role();
             else if (lane == 0)
-                issue_loop(warp == 0 ? 0 : warp == 2 ? 1 : 2);
+                warp == 3 ? scale_loop() : issue_loop(warp == 0 ? 0 : 1);
         } else if (wg == 2) {
             setmaxnreg_dec<Cfg::kRegsWriter>();
             writer_role();
@@ -1112,19 +1452,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             setmaxnreg_inc<Cfg::kRegsEpi>();
             epilogue_role();
         }
-    } else if (warp == 0 || warp == 2 || (kBS && (warp == 3 || warp == 12))) {
-        if (lane == 0) issue_loop(warp == 0 ? 0 : warp == 2 ? 1 : warp == 3 ? 2 : 3);
+    } else if (warp == 0 || warp == 2) {
+        if (lane == 0) issue_loop(warp == 0 ? 0 : 1);
     } else if (warp == 1) {
         mma_role();
+    } else if (kBS && warp == 3) {
+        if (lane == 0) scale_loop();
     } else if (warp >= 8 && warp < 12) {
         writer_role();
     } else if (warp >= 4 && warp < 8) {
         epilogue_role();
     }
+    __syncwarp();
+
+    // Cluster split: the first barrier frees every CTA's operand stages for the pushed
+    // partials (all mainloops are done), the second makes the pushed partials visible
+    // to their owners; the final barrier below is the end of the cluster's work.
+    bool cluster_end = kPair;
+    if constexpr (Cfg::kSplit) {
+        if (p.split > 1) {
+            fence_proxy_async_smem();
+            cluster_sync_all();
+            if (warp >= 4 && warp < 8 && *abort_flag == 0) split_push();
+            __syncwarp();
+            cluster_sync_all();
+            if (warp >= 4 && warp < 8) split_reduce();
+            __syncwarp();
+            cluster_end = true;
+        }
+    }
 
     tc_fence_before_sync();
-    if constexpr (kPair)
-        cluster_sync_all();  // no CTA leaves while its peer may still signal or read it
+    if (cluster_end)
+        cluster_sync_all();  // no CTA leaves while a peer may still signal it or read its memory
     else
         __syncthreads();
     if (warp == 1) {

@@ -29,10 +29,14 @@ gemm_status_t launch_gemm_block_scaled(int64_t M, int64_t N, int64_t K, const vo
                                        const void* C, void* D, int fmt, cudaStream_t stream,
                                        int sms, int dev);
 
-// FP16 with fp32 accumulation whose stream-K scratch is a fixed block inside the
-// module (no allocation); arguments are already validated.
+// FP16 with fp32 accumulation on the stream-K schedule, whose scratch is a fixed block
+// inside the module (no allocation); arguments are already validated.
 gemm_status_t launch_gemm_f16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                                       const void* C, void* D, cudaStream_t stream, int sms, int dev);
+
+// Loads the fixed block of launch_gemm_f16_noalloc on device `dev` (the current
+// device); false if that fails.  Called once per device, on the first accepted call.
+bool setup_fixed_scratch(int dev);
 
 gemm_status_t launch_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
                                const void* C, void* D, cudaStream_t stream, int sms, int dev);

@@ -305,5 +305,15 @@ TN_LAYOUT_HD constexpr uint64_t umma_smem_desc_kmajor(uint32_t saddr, int row_by
            static_cast<uint64_t>(umma_swizzle_mode(row_bytes)) << 61;
 }
 
+// Descriptor of an unswizzled K-major tile (layout type 0) of 8-row x 16-byte core
+// matrices: start address / 16 (bits 0-13), leading byte offset / 16 (bits 16-29:
+// between core matrices along K), stride byte offset / 16 (bits 32-45: between 8-row
+// groups), version 1 (bit 46).  A 32-row x 16-byte tile stored row after row has
+// stride 128 and a single core matrix along K.
+TN_LAYOUT_HD constexpr uint64_t umma_smem_desc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16 |
+           static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32 | static_cast<uint64_t>(1) << 46;
+}
+
 }  // namespace layout
 }  // namespace tn

@@ -81,13 +81,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Contiguous (non-tensor) bulk copy global -> this CTA's shared memory, completion
-// signalled on `bar` as transaction bytes.  Both addresses 16-byte aligned, `bytes`
-// a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
+// 2-D tiled load of one box multicast to the CTAs of `cta_mask` in the cluster: the
+// box lands at the same shared-memory offset `dst` in each, and each CTA's barrier at
+// offset `bar` receives the transaction bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                                      int32_t y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
 }
 
 // 2-D tiled store of one box from shared memory (bulk async-group completion).
@@ -171,6 +174,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      bar)
                  : "memory");
+}
+
+// Copy a 32-row x 128-bit tile from shared memory (descriptor `sdesc`) into TMEM
+// columns taddr .. taddr+3 of lanes 0-31, replicated to the four 32-lane partitions
+// (lanes 32p .. 32p+31): tcgen05.cp .32x128b with .warpx4.  Executed in issue order with
+// this thread's later tcgen05.mma; completion is tracked by tcgen05.commit.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // D(tmem) = A(smem) x B(smem)^T (+ D if accumulate), FP16/BF16 inputs.
@@ -318,7 +329,23 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-// All threads of both CTAs.
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// 16-byte store into the shared memory of a CTA of the cluster (a cluster address
+// from mapa_shared).
+__device__ __forceinline__ void st_shared_cluster_u4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
+                                                     uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// All threads of every CTA of the cluster: shared-memory writes before the barrier
+// (release) are visible to every CTA's reads after it (acquire).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile(
         "barrier.cluster.arrive.release.aligned;\n\t"
@@ -332,8 +359,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 
 // Arrive on an mbarrier that may live in the peer CTA, without release semantics.
-// Used only where the data being signalled is TMEM content whose writes have
-// already completed (tcgen05.wait::st) and been ordered by tcgen05.fence.
+// Used only where what is signalled is TMEM traffic, not generic memory: scale stores
+// completed by tcgen05.wait::st, or accumulator loads completed by tcgen05.wait::ld.
+// The PTX ISA orders tcgen05 operations of two threads through a thread
+// synchronization bracketed by tcgen05.fence::before_thread_sync in the signalling
+// thread (after its wait::st / wait::ld) and tcgen05.fence::after_thread_sync in the
+// waiting thread (before its tcgen05.mma); the mbarrier arrive / wait pair is that
+// synchronization, and its release / acquire semantics concern generic memory only
+// (memory consistency model: tcgen05 operations, and the mbarrier's .sem qualifier).
+// A release.cluster arrive cost about 1000 cycles per use on GB300.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -344,6 +378,20 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking parity test with cluster-scope acquire: whether the phase of the given
+// parity has completed.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -383,6 +431,12 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) 
             bar),
         "h"(cta_mask)
         : "memory");
+}
+
+// The CTA-pair form: issued by the leader, each CTA's tile (same shared-memory offset)
+// goes to that CTA's TMEM.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

@@ -16,19 +16,14 @@
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller; the
  *     library never frees or keeps caller memory.
- *   - Scratch: when the output tiles do not fill whole rounds of the device's
- *     SMs, fp32 accumulation uses a stream-K schedule (units split the k-blocks
- *     of the tiles evenly; a tile cut between units is summed through fp32
- *     partials in scratch memory).  That scratch (64 KB per SM at most, about
- *     9.5 MiB on 152 SMs) is taken with cudaMallocFromPoolAsync on `stream`
- *     from a per-device memory pool the library creates on first need, and
- *     returned to the pool with cudaFreeAsync on `stream` after the kernel; the
- *     pool keeps its memory for later calls until the process exits.  NVFP4
- *     calls of gemm_block_scaled also take, from the same pool and for the same
- *     duration, a copy of SFA and SFB regrouped into contiguous 2 KB blocks (one
- *     per 128 rows and 16 scale bytes; about the size of SFA plus SFB), written
- *     by a small kernel launched on `stream` before the GEMM.  A failed
- *     allocation returns GEMM_ERR_CUDA and launches nothing.
+ *   - No call allocates, frees or resizes device memory; none needs memory beyond the
+ *     caller's operands.  Skinny problems, whose output tiles would leave more than
+ *     half of the device's SMs idle, are split inside thread-block clusters: each
+ *     tile goes to a cluster of up to 8 CTAs that share its k-blocks, and the cluster
+ *     adds its fp32 partial sums in its own shared memory (distributed shared memory)
+ *     before rounding.  Calls on different streams may therefore run concurrently.
+ *     (gemm_f16_noalloc keeps a different, stream-K, schedule over a fixed block of
+ *     the library's own device memory; see there.)
  *   - Matrices are dense and row-major with no padding: A rows are K elements
  *     long (NVFP4: K/2 bytes), B rows likewise, C and D rows are N elements.
  *     Scale-factor matrices are row-major u8 [rows][K / K_blk].
@@ -47,10 +42,11 @@
  *
  * Numerics: products are formed by the tensor cores
  * and summed in fp32 (GEMM_ACC_F32) or fp16 (GEMM_ACC_F16); C is added in fp32
- * and the result rounded once, to nearest even, to the output type.  Under the
- * stream-K schedule the fp32 sum of a cut tile is formed piecewise (contiguous
- * k-ranges, added in fp32), so the order of the fp32 additions depends on M, N,
- * K and the SM count; results are deterministic for a given device and shape.
+ * and the result rounded once, to nearest even, to the output type.  When a tile
+ * is split (inside a cluster, or by gemm_f16_noalloc's stream-K schedule) its fp32
+ * sum is formed piecewise (contiguous k-ranges, added in fp32 in a fixed order), so
+ * the order of the fp32 additions depends on M, N, K and the SM count; results are
+ * deterministic for a given device and shape.
  */
 #ifndef TN_GEMM_H
 #define TN_GEMM_H
@@ -132,25 +128,32 @@ gemm_status_t gemm_fp8(int64_t M, int64_t N, int64_t K, const void *A, const voi
                        const void *C, void *D, int fmt, cudaStream_t stream);
 
 /*
- * FP16 TN GEMM with fp32 accumulation that allocates nothing.
+ * FP16 TN GEMM with fp32 accumulation on a fixed scratch block.
  *
  * The pages have no counterpart of this call: it exists for callers that must
  * not allocate device memory while they run.  Examples are a plugin inside a
  * host application that owns all device memory and hands out only the buffers
  * it chose, a serving loop that has reserved nearly all of HBM up front (so
  * any later allocation may fail), and code whose latency budget cannot absorb
- * an allocation.  gemm_f16 takes its stream-K scratch from a memory pool; this
- * call instead uses a fixed 20 MiB block that is part of the library's module
- * and that every GPU which loads the library holds until the process exits.
+ * an allocation.  gemm_f16 allocates nothing either; this call differs in its
+ * schedule for skinny problems: stream-K, where every SM takes an equal share of
+ * the k-blocks of the last tiles and the unit that finishes a tile adds the
+ * others' fp32 partials from global memory.  Those partials live in a fixed
+ * 20 MiB block that is part of the library's module and that every GPU which
+ * loads the library holds until the process exits.  Stream-K uses every SM even
+ * for a handful of tiles with very long K, where a cluster of 8 would leave most
+ * of the device idle.
  *
  *   M, N, K, A, B, C, D, stream   as gemm_f16 (fp32 accumulation); the result
  *                agrees with gemm_f16's within the fp32 accumulation tolerance
- *                (on one device the two choose the same schedule).
+ *                (the two may split a tile differently).  K <= 32 takes the same
+ *                narrow-K instances as gemm_f16 (one k-block, never split).
  * Scratch limits:
- *   - The call never calls cudaMalloc, cudaFree or a pool allocator.  Its first
- *     call on a device looks up the block's device address there (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *   - The call never calls cudaMalloc, cudaFree or a pool allocator.  The block
+ *     is loaded on a device by the first accepted call of any entry point of this
+ *     library there (which also looks up its device address, once per device,
+ *     with that device current): make one call on each device before reserving
+ *     the rest of its memory and before any stream capture.
  *   - A stream-K launch (128 x 128 tiles on single CTAs) needs 64 KB of fp32
  *     partials per SM it runs on, plus flags: 9.5 MiB on a 152-SM GB300.  A
  *     launch whose need exceeds the 20 MiB block (a device of more than 319

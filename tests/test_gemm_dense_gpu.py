@@ -43,8 +43,8 @@ def test_bf16_in_place():
     P.check(prob, D.cpu(), mode="exact")
 
 
-def test_bf16_stream_k_integers_bit_exact():
-    # 10 tiles of 128 x 256 for a 152-SM device, 256 k-blocks: split between units
+def test_bf16_split_integers_bit_exact():
+    # a few tiles for a 152-SM device, 256 k-blocks: each tile split over a cluster of CTAs
     prob = inputs.make_problem("bf16", 128, 2560, 16384, seed=32, dist="int2", with_c=True)
     P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 16, seed=1), mode="exact")
 
@@ -73,8 +73,8 @@ def test_fp8_ragged_shapes_tolerance(kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind", FP8)
-def test_fp8_stream_k_integers_bit_exact(kind):
-    # 8 tiles of 128 x 256, 256 k-blocks of 128: split between units
+def test_fp8_split_integers_bit_exact(kind):
+    # a few tiles, 256 k-blocks of 128: each tile split over a cluster of CTAs
     prob = inputs.make_problem(kind, 128, 2048, 32768, seed=33, dist="int", with_c=True)
     P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 12, seed=3), mode="exact")
 
@@ -118,8 +118,9 @@ def test_guard_bands_untouched(kind, M, N, K):
     P.check(prob, D.cpu(), mode="exact")
 
 
-def test_concurrent_stream_k_calls_on_two_streams():
-    # two split launches in flight at once take separate scratch from the pool
+def test_concurrent_split_calls_on_two_streams():
+    # two split launches in flight at once on two streams: a split keeps its partials in
+    # its own clusters' shared memory, so concurrent calls share nothing
     probs = [inputs.make_problem("f16", 128, 2560, 16384, seed=63 + i, dist="int2", with_c=True) for i in range(2)]
     dev = P.device()
     gs = [P.to_device(p, dev) for p in probs]

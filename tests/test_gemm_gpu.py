@@ -237,21 +237,21 @@ def test_mxfp8_128x16384_full_size_sampled_rows():
     assert torch.isfinite(D.float()).all()
 
 
-# ------------------------------------------------------------------ stream-K schedule
-# Skinny shapes with long K, whose whole tiles would leave most of the device
-# idle: the fp32 kinds split each tile's k-blocks between several units (with
-# 60..152 units these all take the stream-K schedule, each tile cut into two or
-# more pieces, so owners add one or several partials).  Integer-valued inputs
-# keep every fp32 partial sum exact, so the piecewise sum must match bit for bit.
+# ------------------------------------------------------------------ split schedules
+# Skinny shapes with long K, whose whole tiles would leave most of the device idle:
+# the fp32 kinds give each tile to a cluster of up to 8 CTAs that split its k-blocks
+# and add their fp32 partials through distributed shared memory.  Integer-valued
+# inputs keep every fp32 partial sum exact, so the piecewise sum must match bit for
+# bit.
 
 @pytest.mark.parametrize("M,N,K,with_c", [(128, 2560, 16384, True), (500, 760, 16384, True),
                                           (64, 2056, 24576, False), (1, 4096, 16384, True)])
-def test_stream_k_fp16_integers_bit_exact(M, N, K, with_c):
+def test_split_fp16_integers_bit_exact(M, N, K, with_c):
     prob = inputs.make_problem("f16", M, N, K, seed=M + N + K, dist="int2", with_c=with_c)
     P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 24, seed=1), mode="exact")
 
 
-def test_stream_k_fp16_in_place():
+def test_split_fp16_in_place():
     prob = inputs.make_problem("f16", 300, 520, 16384, seed=21, dist="int2", with_c=True)
     g = P.to_device(prob, P.device())
     D = g["C"].clone()
@@ -261,13 +261,14 @@ def test_stream_k_fp16_in_place():
 
 
 @pytest.mark.parametrize("M,N,K", [(1000, 1000, 16384), (129, 264, 65536)])
-def test_stream_k_fp16_random_tolerance(M, N, K):
+def test_split_fp16_random_tolerance(M, N, K):
     prob = inputs.make_problem("f16", M, N, K, seed=M + K, dist="normal0.1", with_c=True)
     P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 24, seed=2), mode="tol")
 
 
-def test_stream_k_repeatable_across_calls_and_streams():
-    # the scratch pool hands back blocks from earlier calls: results must not depend on them
+def test_split_repeatable_across_calls_and_streams():
+    # a cluster adds its partials in rank order: the result depends on neither the call
+    # nor the stream
     prob = inputs.make_problem("f16", 500, 760, 16384, seed=22, dist="normal0.1", with_c=True)
     first = P.run_gpu(prob, accum=0)
     s = torch.cuda.Stream()
@@ -277,18 +278,18 @@ def test_stream_k_repeatable_across_calls_and_streams():
 
 
 @pytest.mark.parametrize("M,N,K,with_c", [(128, 2048, 65536, True), (100, 3000, 65536, False)])
-def test_stream_k_nvfp4_integers_bit_exact(M, N, K, with_c):
+def test_split_nvfp4_integers_bit_exact(M, N, K, with_c):
     prob = inputs.make_problem("nvfp4", M, N, K, seed=M + N, dist="int", with_c=with_c)
     P.check(prob, P.run_gpu(prob), rows=P.sample_rows(M, 12, seed=3), mode="exact")
 
 
 @pytest.mark.parametrize("M,N,K,with_c", [(100, 2048, 24576, True), (128, 1928, 24576, False)])
-def test_stream_k_mxfp8_integers_bit_exact(M, N, K, with_c):
+def test_split_mxfp8_integers_bit_exact(M, N, K, with_c):
     prob = inputs.make_problem("mxfp8", M, N, K, seed=M + N, dist="int", with_c=with_c)
     P.check(prob, P.run_gpu(prob), rows=P.sample_rows(M, 12, seed=4), mode="exact")
 
 
-def test_stream_k_mxfp8_random_tolerance():
+def test_split_mxfp8_random_tolerance():
     prob = inputs.make_problem("mxfp8", 128, 1024, 49152, seed=23, dist="normal", with_c=True)
     P.check(prob, P.run_gpu(prob), rows=P.sample_rows(128, 12, seed=5), mode="tol")
 
@@ -298,8 +299,8 @@ def test_stream_k_mxfp8_random_tolerance():
 # stay within a few hundred MB of device memory).  Integer inputs keep every fp32
 # partial sum exact, so sampled rows must match bit for bit.
 
-def test_large_k_fp16_single_tile_split_over_all_units():
-    # K = 2^20: one 128 x 256 tile whose 16384 k-blocks are split across every unit
+def test_large_k_fp16_single_tile_split_over_a_cluster():
+    # K = 2^20: one 128 x 128 tile whose 16384 k-blocks are split over a cluster of 8 CTAs
     prob = inputs.make_problem("f16", 128, 128, 1 << 20, seed=51, dist="int2", with_c=True)
     P.check(prob, P.run_gpu(prob, accum=0), rows=[0, 1, 63, 127], mode="exact")
 

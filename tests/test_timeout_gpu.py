@@ -8,8 +8,8 @@ GEMM_ERR_TIMEOUT, the other CTA's tile is still computed exactly, and the CUDA
 context stays usable.
 
 The test build runs in a child process: two copies of the library (each with
-its own static CUDA runtime) cannot be used in one process.  The FP16 case has two
-single-CTA tiles; the NVFP4 case (two 128 x 128 tiles) also exercises the abandon
+its own static CUDA runtime) cannot be used in one process.  The FP16 case has
+single-CTA tiles; the FP16 split case gives each tile to a cluster of CTAs; the NVFP4 case (two 128 x 128 tiles) also exercises the abandon
 path of the scale issuers and scale writers; the NVFP4 pair case (40 tiles of
 256 x 256, one per CTA pair) that of the CTA-pair instance.
 """
@@ -49,13 +49,14 @@ CHILD = textwrap.dedent(r"""
     kind = sys.argv[3]
     dev = torch.device("cuda", 0)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    if kind == "f16":
-        prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    if kind in ("f16", "f16split"):
+        M, N, K = (128, 512, 256) if kind == "f16" else (128, 2048, 4096)
+        prob = inputs.make_problem("f16", M, N, K, seed=31, dist="int2", with_c=False)
         A, B = prob["A"].to(dev), prob["B"].to(dev)
-        D = torch.zeros(128, 512, dtype=torch.float16, device=dev)
+        D = torch.zeros(M, N, dtype=torch.float16, device=dev)
         torch.cuda.synchronize()
         t0 = time.time()
-        rc = lib.gemm_f16(128, 512, 256, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 0, stream)
+        rc = lib.gemm_f16(M, N, K, A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 0, stream)
     else:
         M, N, K, seed = (128, 256, 512, 32) if kind == "nvfp4" else (1024, 2560, 512, 33)
         prob = inputs.make_problem("nvfp4", M, N, K, seed=seed, dist="int", with_c=False)
@@ -76,8 +77,11 @@ CHILD = textwrap.dedent(r"""
 """)
 
 
-# (kind, the tile of the first unit: the withheld stage affects only that tile)
-CASES = [("f16", (128, 256)), ("nvfp4", (128, 128)), ("nvfp4pair", (256, 256))]
+# (kind, the tile of the first unit: the withheld stage affects only that tile).  In
+# "f16split" the first unit is CTA 0 of the first tile's cluster (128 x 2048 x 4096 FP16:
+# eight 128 x 256 tiles, each split over a cluster): its CTA gives up, the cluster
+# still meets at its barriers, and only that tile is affected.
+CASES = [("f16", (128, 256)), ("f16split", (128, 256)), ("nvfp4", (128, 128)), ("nvfp4pair", (256, 256))]
 
 
 @pytest.mark.parametrize("kind,tile0", CASES, ids=[c[0] for c in CASES])
@@ -101,6 +105,8 @@ def test_bounded_wait_runs_out_and_is_reported(kind, tile0):
     assert res["usable"]
     if kind == "f16":
         prob = inputs.make_problem("f16", 128, 512, 256, seed=31, dist="int2", with_c=False)
+    elif kind == "f16split":
+        prob = inputs.make_problem("f16", 128, 2048, 4096, seed=31, dist="int2", with_c=False)
     elif kind == "nvfp4":
         prob = inputs.make_problem("nvfp4", 128, 256, 512, seed=32, dist="int", with_c=False)
     else:
