@@ -107,13 +107,15 @@ def workload_bytes(w) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while the GPU is busy."""
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU is busy (every
+    `period_ms`, each sample time-stamped so that it can be matched to a timed window)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
 
@@ -121,7 +123,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
@@ -136,17 +138,35 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
-        rows = []
+    def rows(self):
+        import datetime
+        out = []
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 10:
+            if len(f) < 11:
                 continue
             try:
-                rows.append({"sm": float(f[1]), "max": float(f[2]), "util": float(f[4]),
-                             "hw": f[6], "hwt": f[7], "swt": f[8], "pcap": f[9]})
+                t = datetime.datetime.strptime(f[10], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                out.append({"sm": float(f[1]), "max": float(f[2]), "util": float(f[4]),
+                            "hw": f[6], "hwt": f[7], "swt": f[8], "pcap": f[9], "t": t})
             except ValueError:
                 continue
+        return out
+
+    def median_mhz(self, t0: float, t1: float):
+        """Median SM clock of the samples taken between host times t0 and t1 (the sample
+        nearest to the window's middle if none falls inside)."""
+        rows = self.rows()
+        if not rows:
+            return None
+        inside = [r["sm"] for r in rows if t0 <= r["t"] <= t1]
+        if inside:
+            return statistics.median(inside)
+        mid = 0.5 * (t0 + t1)
+        return min(rows, key=lambda r: abs(r["t"] - mid))["sm"]
+
+    def summary(self):
+        rows = self.rows()
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
         busy = [r for r in rows if r["util"] > 50] or rows
@@ -274,9 +294,12 @@ def vendor_arm(args):
         return
     peaks, peak_src = load_peaks()
     with ClockSampler(0) as clocks:
-        ms = time_steps(runner, args.steps, stream, graph=not args.no_graph) / args.steps
+        reps = time_repeats(runner, args.steps, stream, args.repeats, graph=not args.no_graph)
+    ms = statistics.median(r[0] for r in reps) / args.steps
+    rl = roofline(w, ms, peaks, peak_src)
+    rl["traffic"] = None  # the recorded DRAM traffic belongs to this library's kernel
     print(json.dumps({"impl": "vendor", "workload": w.name, "ms_per_step": round(ms, 5),
-                      "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2), "roofline": roofline(w, ms, peaks, peak_src),
+                      "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2), "roofline": rl,
                       "clocks": clocks.summary(),
                       "note": "cuBLAS through torch; block-scaled and FP8 calls add no C"}), flush=True)
 
@@ -314,6 +337,39 @@ def time_steps(runner, steps: int, stream, graph: bool = True) -> float:
         end.record(stream)
     end.synchronize()
     return start.elapsed_time(end)
+
+
+def time_repeats(runner, steps: int, stream, repeats: int, graph: bool = True):
+    """The timed region -- `steps` back-to-back launches, captured once into a CUDA graph
+    (graph=True) -- run `repeats` times, each bracketed by CUDA events on `stream` and a
+    synchronize.  Returns [(ms, host_t0, host_t1)] per repeat; the host times let the
+    clock samples be matched to each repeat."""
+    import torch
+    out = []
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                runner.launch(i)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+    for _ in range(repeats):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            if g is not None:
+                g.replay()
+            else:
+                for i in range(steps):
+                    runner.launch(i, stream)
+            end.record(stream)
+        end.synchronize()
+        out.append((start.elapsed_time(end), t0, time.time()))
+    return out
 
 
 def peak_for(w, peaks):
@@ -519,10 +575,16 @@ def gpu_arm(args):
             time_steps(runner, 20, stream, graph=False)
         barrier()
         torch.cuda.synchronize()
-        ms_total = time_steps(runner, args.steps, stream, graph=not args.no_graph)
+        reps = time_repeats(runner, args.steps, stream, 1 if args.quick else args.repeats, graph=not args.no_graph)
         torch.cuda.synchronize()
         barrier()
-    ms = reduce_max(ms_total / args.steps, world, dev)
+    rep_ms = [r[0] / args.steps for r in reps]
+    ms = reduce_max(statistics.median(rep_ms), world, dev)
+    repeats = []
+    for (total, t0, t1), m in zip(reps, rep_ms):
+        mhz = clocks.median_mhz(t0, t1)
+        repeats.append({"ms_per_step": round(m, 5), "sm_mhz": mhz,
+                        "us_x_ghz": round(m * 1e3 * mhz / 1e3, 2) if mhz else None})
     assert runner.tg.gemm_last_device_error() == runner.tg.GEMM_OK
 
     if args.quick:  # profiling runs: only the W + K launches above
@@ -551,8 +613,13 @@ def gpu_arm(args):
                 "method": "per step: pinned host -> device copy of A, B (and C / scales), the GEMM, device -> "
                           "pinned host read of D; steps pipelined over the device buffer sets (copies of "
                           "step i+1, GEMM of step i and read of step i-1 overlap on three streams)"},
-        "gpu_launches": args.steps,
-        "timing": "CUDA-graph replay of the K launches" if not args.no_graph else "back-to-back launches",
+        "gpu_launches": args.steps * len(reps),
+        "timing": (f"{args.repeats} repeats of the K launches ("
+                   + ("CUDA-graph replay" if not args.no_graph else "back-to-back launches")
+                   + "); value and ms_per_step from the median repeat"),
+        "repeats": repeats,
+        "repeat_spread": {"min_ms": round(min(rep_ms), 5), "median_ms": round(statistics.median(rep_ms), 5),
+                          "max_ms": round(max(rep_ms), 5)},
     }
     if rank == 0 and world == 1 and not args.no_extras:
         extras = {}
@@ -632,6 +699,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed regions of K steps each (value: the median one); clocks sampled per repeat")
     ap.add_argument("--workload", default="fp16_4096")
     ap.add_argument("--impl", choices=["ours", "reference", "vendor"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' lines")

@@ -119,6 +119,10 @@ struct Params {
     // CTA a share of the tile's 32-row chunks, the partials in rank order), add C,
     // round once and store.  No global scratch is involved.
     int split;
+    // L2 prefetch distance of the B issuer, in k-blocks (0 = off): for problems bound by
+    // streaming B from memory, each B box is also requested into L2 this many k-blocks
+    // ahead of its load into shared memory.
+    int b_prefetch;
 };
 
 // How the block-scaled kinds move their scale factors (Config::SF_MODE).
@@ -664,6 +668,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
                     tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
+                }
+                if (role == 1 && p.b_prefetch > 0) {
+                    // the first k-blocks of the segment are requested at its start
+                    if (kb == k0)
+                        for (int f = k0 + 1; f < k1 && f <= k0 + p.b_prefetch; ++f)
+                            tma_prefetch_l2_2d(&tmB, f * Cfg::kKCoordPerStage, n0);
+                    if (kb + p.b_prefetch + 1 < k1)
+                        tma_prefetch_l2_2d(&tmB, (kb + p.b_prefetch + 1) * Cfg::kKCoordPerStage, n0);
                 }
                 ++loads[s];
                 if (++s == STAGES) {
@@ -1325,12 +1337,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // keeps, in its idle operand stages, one fp32 slot per (owned chunk, source CTA):
     // slot (k, s) at k * S + s, [col/4][lane][4] inside.
     constexpr int UNIT_BYTES = 32 * Cfg::EPI_COLS * 4;
-    // split_push (after every CTA of the cluster is past its mainloop): epilogue warp q
-    // reads its lane quarter of the accumulator chunk by chunk and stores each chunk into
-    // the owner's slot for this CTA through distributed shared memory.
+    // split_push (after every CTA of the cluster is past its mainloop), by every warp of
+    // the CTA: warp w reads lane quarter w % 4 of the accumulator (the quarter a warp may
+    // access) for the column chunks g with g % (warps / 4) == w / 4, and stores each
+    // chunk into its owner's slot for this CTA -- through distributed shared memory, or
+    // directly when this CTA owns the chunk.
     auto split_push = [&]() {
         if constexpr (Cfg::kSplit) {
             constexpr int EC = Cfg::EPI_COLS;
+            constexpr int GROUPS = Cfg::THREADS / 128;  // warps per lane quarter
             const int q = warp & 3;
             const int S = p.split;
             const int r = static_cast<int>(blockIdx.x) % S;
@@ -1339,20 +1354,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc_fence_after_sync();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-            for (int g = 0; g < BN / EC; ++g) {
+            for (int g = warp >> 2; g < BN / EC; g += GROUPS) {
                 const int u = 4 * g + q;
                 const int owner = u % S, k = u / S;
                 uint32_t v[EC];
                 load_chunk<EC>(tacc, g * EC, v);
                 tmem_ld_wait();
-                const uint32_t dst = mapa_shared(
-                    sbase + Cfg::OFF_A + static_cast<uint32_t>((k * S + r) * UNIT_BYTES + lane * 16),
-                    static_cast<uint32_t>(owner));
+                if (none)
 #pragma unroll
-                for (int i = 0; i < EC / 4; ++i) {
-                    if (none)
-                        st_shared_cluster_u4(dst + i * 512, 0u, 0u, 0u, 0u);
-                    else
+                    for (int i = 0; i < EC; ++i) v[i] = 0u;
+                const uint32_t off = static_cast<uint32_t>(Cfg::OFF_A + (k * S + r) * UNIT_BYTES + lane * 16);
+                if (owner == r) {
+#pragma unroll
+                    for (int i = 0; i < EC / 4; ++i)
+                        *reinterpret_cast<uint4*>(smem + off + i * 512) =
+                            make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                } else {
+                    const uint32_t dst = mapa_shared(sbase + off, static_cast<uint32_t>(owner));
+#pragma unroll
+                    for (int i = 0; i < EC / 4; ++i)
                         st_shared_cluster_u4(dst + i * 512, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
             }
@@ -1467,24 +1487,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     // Cluster split: the first barrier frees every CTA's operand stages for the pushed
     // partials (all mainloops are done), the second makes the pushed partials visible
-    // to their owners; the final barrier below is the end of the cluster's work.
-    bool cluster_end = kPair;
+    // to their owners.  No CTA touches another's shared memory after it, so each CTA
+    // finishes on its own.
     if constexpr (Cfg::kSplit) {
         if (p.split > 1) {
             fence_proxy_async_smem();
             cluster_sync_all();
-            if (warp >= 4 && warp < 8 && *abort_flag == 0) split_push();
+            if (*abort_flag == 0) split_push();
             __syncwarp();
             cluster_sync_all();
             if (warp >= 4 && warp < 8) split_reduce();
             __syncwarp();
-            cluster_end = true;
         }
     }
 
     tc_fence_before_sync();
-    if (cluster_end)
-        cluster_sync_all();  // no CTA leaves while a peer may still signal it or read its memory
+    if constexpr (kPair)
+        cluster_sync_all();  // no CTA leaves while its peer may still signal it or read its memory
     else
         __syncthreads();
     if (warp == 1) {
