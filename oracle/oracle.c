@@ -36,6 +36,8 @@
  *     subnormals, S.1111.111 is NaN, no Inf, max 448), E5M2 (bias 15, two
  *     mantissa bits, subnormals, exponent 31 is Inf or NaN as in IEEE 754),
  *     E8M0 (2^(e-127), 0xFF is NaN).  BF16 is the upper half of an IEEE fp32.
+ *     E2M1 is decoded by its table of magnitudes; E4M3, E5M2 and E8M0 by 256-entry
+ *     tables filled once from those bit-field definitions.
  *   - FP4 packing: element 2j sits in the low nibble of byte j, element 2j+1
  *     in the high nibble (the pages' "lower slot = low 16 bits" packing rule
  *     for two halves in one 32-bit operand, carried over to two nibbles).
@@ -86,8 +88,9 @@ double oracle_e2m1_to_f64(uint8_t code) {
     return (code & 8) ? -v : v;
 }
 
-/* E4M3 ("fn" variant) from its bit fields: bias 7, 3 mantissa bits. */
-double oracle_e4m3_to_f64(uint8_t code) {
+/* E4M3 ("fn" variant) from its bit fields: bias 7, 3 mantissa bits.  This builds the
+ * decode table; the GEMMs look codes up in it (e4m3_table). */
+static double e4m3_from_fields(uint8_t code) {
     int s = code >> 7, e = (code >> 3) & 0xf, m = code & 7;
     double v;
     if (e == 15 && m == 7)
@@ -99,8 +102,9 @@ double oracle_e4m3_to_f64(uint8_t code) {
     return s ? -v : v;
 }
 
-/* E5M2 from its bit fields: bias 15, 2 mantissa bits, IEEE-style Inf / NaN. */
-double oracle_e5m2_to_f64(uint8_t code) {
+/* E5M2 from its bit fields: bias 15, 2 mantissa bits, IEEE-style Inf / NaN (builds
+ * the decode table). */
+static double e5m2_from_fields(uint8_t code) {
     int sign = code >> 7, exp = (code >> 2) & 0x1f, man = code & 3;
     double v;
     if (exp == 31)
@@ -112,11 +116,46 @@ double oracle_e5m2_to_f64(uint8_t code) {
     return sign ? -v : v;
 }
 
-/* E8M0: a pure power of two, 2^(code - 127); 0xFF is NaN. */
-double oracle_e8m0_to_f64(uint8_t code) {
+/* E8M0: a pure power of two, 2^(code - 127); 0xFF is NaN (builds the decode table). */
+static double e8m0_from_fields(uint8_t code) {
     if (code == 0xff)
         return NAN;
     return ldexp(1.0, (int)code - 127);
+}
+
+/* The 8-bit formats are decoded by table: every code's value, filled once from the
+ * bit-field definitions above (E2M1 uses its listed magnitudes, E2M1_MAG). */
+static double E4M3_TABLE[256], E5M2_TABLE[256], E8M0_TABLE[256];
+static int tables_ready = 0;
+
+static void build_tables(void) {
+    for (int c = 0; c < 256; ++c) {
+        E4M3_TABLE[c] = e4m3_from_fields((uint8_t)c);
+        E5M2_TABLE[c] = e5m2_from_fields((uint8_t)c);
+        E8M0_TABLE[c] = e8m0_from_fields((uint8_t)c);
+    }
+    tables_ready = 1;
+}
+
+static void ensure_tables(void) {
+#pragma omp critical(oracle_tables)
+    if (!tables_ready)
+        build_tables();
+}
+
+double oracle_e4m3_to_f64(uint8_t code) {
+    ensure_tables();
+    return E4M3_TABLE[code];
+}
+
+double oracle_e5m2_to_f64(uint8_t code) {
+    ensure_tables();
+    return E5M2_TABLE[code];
+}
+
+double oracle_e8m0_to_f64(uint8_t code) {
+    ensure_tables();
+    return E8M0_TABLE[code];
 }
 
 /* ---------------------------------------------------------------- rounding */
@@ -203,13 +242,13 @@ static double low_element(int fmt, const uint8_t *X, int64_t K, int64_t r, int64
         uint8_t code = (k % 2 == 0) ? (byte & 0xf) : (byte >> 4);
         return oracle_e2m1_to_f64(code);
     }
-    return oracle_e4m3_to_f64(X[r * K + k]);
+    return E4M3_TABLE[X[r * K + k]];
 }
 
 static double scale_factor(int fmt, const uint8_t *SF, int64_t K, int64_t r, int64_t sfk) {
     int64_t kblk = (fmt == 0) ? 16 : 32;
     uint8_t code = SF[r * (K / kblk) + sfk];
-    return (fmt == 0) ? oracle_e4m3_to_f64(code) : oracle_e8m0_to_f64(code);
+    return (fmt == 0) ? E4M3_TABLE[code] : E8M0_TABLE[code];
 }
 
 /*
@@ -229,6 +268,7 @@ int oracle_gemm_block_scaled(int fmt, int64_t M, int64_t N, int64_t K, const uin
         return -1;
     if (rows == NULL)
         nrows = M;
+    ensure_tables();
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < nrows; ++i) {
         int64_t m = rows ? rows[i] : i;
@@ -256,8 +296,8 @@ static double dense_element(int fmt, const void *X, int64_t idx) {
     switch (fmt) {
         case FMT_FP16: return oracle_f16_to_f64(((const uint16_t *)X)[idx]);
         case FMT_BF16: return oracle_bf16_to_f64(((const uint16_t *)X)[idx]);
-        case FMT_E4M3: return oracle_e4m3_to_f64(((const uint8_t *)X)[idx]);
-        default: return oracle_e5m2_to_f64(((const uint8_t *)X)[idx]);
+        case FMT_E4M3: return E4M3_TABLE[((const uint8_t *)X)[idx]];
+        default: return E5M2_TABLE[((const uint8_t *)X)[idx]];
     }
 }
 
@@ -276,6 +316,7 @@ int oracle_gemm_dense(int a_fmt, int b_fmt, int out_fmt, int64_t M, int64_t N, i
         return -1;
     if (rows == NULL)
         nrows = M;
+    ensure_tables();
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < nrows; ++i) {
         int64_t m = rows ? rows[i] : i;
