@@ -59,12 +59,16 @@ inline bool would_split(int64_t M, int64_t N, int64_t K, int k_per_block, int sm
 }
 
 // Dense kinds: CTA pairs (256 x 256 tiles) once their tiles fill every SM pair at least
-// once; below that the single-CTA instances (128 x 256, or 128 x 128 with stream-K, or
-// 128 x 64) spread the work over twice as many units.  Measured on GB300 (FP16, no C):
-// 512 x 8192 x 2048 14.5 -> 13.9 us, 2048^2 x 1024 10.0 -> 9.2, 256 x 2048 x 8192
-// 26.5 -> 22.8; 4096^2 x 1024 (256 pair tiles) stays on pairs.
-inline bool use_pairs(int64_t M, int64_t N, int sms) {
-    return M > 128 && ((M + 255) / 256) * ((N + 255) / 256) >= sms / 2;
+// once, or at least half of the SM pairs when K >= 2048; below that the single-CTA
+// instances spread the work over twice as many units.  A single CTA loads 48 KB of
+// operands per 128-byte k-block against 32 KB per CTA of a pair, so long-K problems
+// favour pairs even with a few SM pairs idle.  Measured on GB300 (FP16, no C):
+// 2048^2 x 4096 (64 pair tiles) 27.2 -> 24.4 us and 512 x 8192 x 2048 17.5 -> 15.7 us on
+// pairs, but 2048^2 x 1024 9.4 -> 9.8 us, so short K keeps single CTAs; 4096^2 x 1024
+// (256 pair tiles) runs on pairs.
+inline bool use_pairs(int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    return M > 128 && (pair_tiles >= sms / 2 || (K >= 2048 && 2 * pair_tiles >= sms / 2));
 }
 
 // Small problems: whole tiles of `big` would keep fewer than half of the units busy,
@@ -91,7 +95,7 @@ enum DenseChoice { DENSE_PAIR_256 = 0, DENSE_SINGLE_256 = 1, DENSE_SINGLE_128 = 
 // (The stream-K rule of the fixed-scratch call; dense_plan below is the rule of the
 // calls that split tiles inside clusters.)
 inline DenseChoice dense_choice(int64_t M, int64_t N, int64_t K, int k_per_block, int sms) {
-    if (use_pairs(M, N, sms)) return DENSE_PAIR_256;
+    if (use_pairs(M, N, K, sms)) return DENSE_PAIR_256;
     if (use_small_tiles(M, N, K, k_per_block, sms, kDenseSingle256)) return DENSE_SINGLE_64;
     return would_split(M, N, K, k_per_block, sms, kDenseSingle256) ? DENSE_SINGLE_128 : DENSE_SINGLE_256;
 }
@@ -149,7 +153,7 @@ struct DensePlan {
 // clusters per cluster size of the two instances.
 inline DensePlan dense_plan(int64_t M, int64_t N, int64_t K, int k_per_block, int sms, const int* res256,
                             const int* res128) {
-    if (use_pairs(M, N, sms)) return DensePlan{DENSE_PAIR_256, 1};
+    if (use_pairs(M, N, K, sms)) return DensePlan{DENSE_PAIR_256, 1};
     const int nkb = static_cast<int>((K + k_per_block - 1) / k_per_block);
     const long long t256 = tile_count(M, N, kDenseSingle256), t128 = tile_count(M, N, kDenseSingle128);
     const int s256 = choose_split(t256, nkb, sms, res256);

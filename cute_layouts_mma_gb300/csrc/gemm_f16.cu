@@ -114,7 +114,7 @@ gemm_status_t launch_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, co
             default: return run<CfgF16Acc32>(M, N, K, A, B, C, D, stream, sms, dev, plan.split);
         }
     }
-    return dispatch::use_pairs(M, N, sms) ? run<CfgF16Acc16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
+    return dispatch::use_pairs(M, N, K, sms) ? run<CfgF16Acc16Pair>(M, N, K, A, B, C, D, stream, sms, dev)
                                           : run<CfgF16Acc16>(M, N, K, A, B, C, D, stream, sms, dev);
 }
 

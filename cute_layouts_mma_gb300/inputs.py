@@ -22,6 +22,9 @@ Workloads (name -> recipe):
                       fp32 accumulation, bf16 D.                           seed 5
   fp8e4m3_8192        M=N=K=8192, A,B = E4M3 RNE(clip(N(0,1), +-448)), no
                       scales, C absent, fp32 accumulation, bf16 D.         seed 6
+  mxfp8_8192          M=N=K=8192, as mxfp8_128x16384, C absent.            seed 7
+  fp16_128x4096x4096  M=128, N=K=4096 (a skinny problem: each tile split over a
+                      cluster), as fp16_4096 without C.                    seed 8
 """
 from __future__ import annotations
 
@@ -66,6 +69,7 @@ WORKLOADS = {
         Workload("bf16_4096", KIND_BF16, 4096, 4096, 4096, "normal0.1", True, 0, 5),
         Workload("fp8e4m3_8192", KIND_FP8_E4M3, 8192, 8192, 8192, "normal", False, 0, 6),
         Workload("mxfp8_8192", KIND_MXFP8, 8192, 8192, 8192, "normal", False, 0, 7),
+        Workload("fp16_128x4096x4096", KIND_F16, 128, 4096, 4096, "normal0.1", False, 0, 8),
     ]
 }
 

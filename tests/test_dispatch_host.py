@@ -54,9 +54,9 @@ PLAN_CASES = [
     ((4096, 4096, 1024, 64), (PAIR256, 1)),       # 256 pair tiles: pairs (24.0 against 26.5 us)
     ((256, 256, 256, 64), (SINGLE64, 1)),         # latency-bound: 128 x 64 tiles
     ((1024, 1024, 1024, 64), (SINGLE64, 1)),      # 7.2 us; split in clusters 12.6 us
-    ((2048, 2048, 1024, 64), (SINGLE256, 1)),     # 128 whole tiles fill the device
-    ((512, 8192, 2048, 64), (SINGLE256, 1)),
-    ((2048, 2048, 4096, 64), (SINGLE256, 1)),
+    ((2048, 2048, 1024, 64), (SINGLE256, 1)),     # 64 pair tiles, short K: single CTAs (9.4 against 9.8)
+    ((512, 8192, 2048, 64), (PAIR256, 1)),        # 64 pair tiles, long K: 17.5 -> 15.7 on pairs
+    ((2048, 2048, 4096, 64), (PAIR256, 1)),       # 27.2 -> 24.4 on pairs
     ((1024, 1024, 4096, 64), (SINGLE256, 4)),     # 20.3 -> 14.4
     ((256, 2048, 8192, 64), (SINGLE256, 8)),      # 24.9 -> 16.5
     ((128, 4096, 4096, 64), (SINGLE256, 8)),      # 26.8 -> 12.2
@@ -72,13 +72,13 @@ FIXED_SCRATCH_CASES = [
     ((256, 256, 256, 64), (SINGLE64, 0, 0)),
     ((1024, 1024, 1024, 64), (SINGLE64, 0, 0)),
     ((2048, 2048, 1024, 64), (SINGLE256, 0, 1)),    # 64 pair tiles: single CTAs, whole tiles
-    ((512, 8192, 2048, 64), (SINGLE256, 0, 1)),     # 64 pair tiles: dense single CTAs, block-scaled pairs
+    ((512, 8192, 2048, 64), (PAIR256, 0, 1)),       # 64 pair tiles, long K: pairs
     ((1024, 1024, 4096, 64), (SINGLE128, 0, 0)),    # 256-wide tiles would split: 128-wide, whole
     ((256, 2048, 8192, 64), (SINGLE128, 1, 0)),     # 128-wide with stream-K
     ((128, 2560, 16384, 64), (SINGLE128, 1, 0)),
     ((128, 4096, 4096, 64), (SINGLE256, 0, 0)),     # shares too short to split: whole tiles
     ((128, 16384, 8192, 128), (SINGLE256, 0, 0)),   # the MXFP8 skinny shape; block-scaled: single
-    ((1024, 2560, 8192, 128), (SINGLE256, 0, 1)),   # 40 pair tiles: block-scaled pairs
+    ((1024, 2560, 8192, 128), (PAIR256, 0, 1)),     # 40 pair tiles, long K: pairs (dense and block-scaled)
     ((512, 4096, 8192, 128), (SINGLE256, 0, 0)),    # 32 pair tiles: block-scaled single CTAs
     ((8192, 8192, 8192, 128), (PAIR256, 0, 1)),
 ]
@@ -142,14 +142,15 @@ def test_stream_k_rule_on_single_128(driver, sms):
 
 
 def test_pairs_need_filled_sm_pairs(driver):
-    # dense pairs exactly when the 256 x 256 tiles fill every SM pair (M > 128);
-    # block-scaled pairs from half of them
-    problems = [(M, N, 4096, 64) for M in (128, 256, 1024, 2048, 4096) for N in (256, 2048, 4864, 9728)]
-    for (M, N, _, _), g in zip(problems, choose(driver, problems)):
+    # dense pairs when the 256 x 256 tiles fill every SM pair (M > 128), or half of them
+    # with K >= 2048; block-scaled pairs from half of them
+    problems = [(M, N, K, 64) for M in (128, 256, 1024, 2048, 4096) for N in (256, 2048, 4864, 9728) for K in (1024, 4096)]
+    for (M, N, K, _), g in zip(problems, choose(driver, problems)):
         pair_tiles = -(-M // 256) * -(-N // 256)
-        assert (g[0] == PAIR256) == (M > 128 and pair_tiles >= 76), (M, N)
-        assert (g[3] == PAIR256) == (M > 128 and pair_tiles >= 76), (M, N)
-        assert g[2] == int(M > 128 and 2 * pair_tiles >= 76), (M, N)
+        dense = M > 128 and (pair_tiles >= 76 or (K >= 2048 and 2 * pair_tiles >= 76))
+        assert (g[0] == PAIR256) == dense, (M, N, K)
+        assert (g[3] == PAIR256) == dense, (M, N, K)
+        assert g[2] == int(M > 128 and 2 * pair_tiles >= 76), (M, N, K)
 
 
 def test_raster_group_fits_the_budget(driver):
