@@ -3,11 +3,15 @@
 // FP16, BF16 or FP8, or in the block-scaled NVFP4 / MXFP8 forms ("数据布局及其记号",
 // block-scaled MMA section).
 //
-// Work is dealt to persistent units (CTAs, or CTA pairs) either as whole tiles,
-// round robin, or -- for skinny problems that would leave most units idle -- as a
-// stream-K split of the tiles' k-blocks (see Params).  The set-up overlaps the
-// previous launch on the stream (programmatic dependent launch); global memory is
-// touched only after griddepcontrol.wait.
+// Work is dealt to persistent units (CTAs, or CTA pairs) as whole tiles, round
+// robin; for skinny problems that would leave most SMs idle, each tile instead goes
+// to a cluster of up to 8 CTAs that split its k-blocks and add their partial sums
+// through distributed shared memory (the cluster split, see Params).  A launch
+// overlaps the previous one on the stream (programmatic dependent launch): the
+// set-up and each role's own bookkeeping run at once, and a thread waits for the
+// previous grid (griddepcontrol.wait) only right before its first global-memory
+// access -- the TMA issuers before their first load, the epilogue warps before
+// theirs; the MMA issuer and the scale writers touch no global memory.
 //
 // Output tiles are (128 * PAIR) x BN.  With PAIR = 2 the two CTAs of a (2,1,1)
 // cluster share a tile: CTA r loads A rows 128r .. 128r+127 and B rows
@@ -24,11 +28,10 @@
 //                peer's copies signal the leader's barrier directly).  A TMA
 //                instruction occupies its issuing warp for a few hundred cycles
 //                whatever the box size, so each operand stream has its own warp.
-//   warps 3, 12  (block-scaled only) issuers of the raw scale boxes (this CTA's
-//                128 SFA rows, all BN SFB rows of the tile) on `sf_full`: TMA boxes
-//                of the row-major scales, or (NVFP4, and MXFP8 in CTA pairs) bulk
-//                copies of packed blocks.  In the register-drain layout warp 3 issues
-//                both.
+//   warp 3       (block-scaled only) issuer of the scale boxes: TMA boxes of the
+//                caller's row-major SFA (this CTA's 128 rows) and SFB (the tile's BN
+//                rows; in NVFP4 CTA pairs each CTA loads half and multicasts it to
+//                both) into the scale slots.
 //   warp 1       TMEM allocation; in the leader, the MMA issuer (one thread):
 //                tcgen05.mma into a TMEM accumulator, 32 bytes of K per MMA;
 //                tcgen05.commit frees the stage (`empty`, in both CTAs) and, at the
@@ -36,7 +39,7 @@
 //                (`tmem_full`, in both CTAs).
 //   warps 4-7    epilogue (and 12-15 in the register-drain layout): tcgen05.ld
 //                of the accumulator (warp w reads TMEM lanes 32*(w%4) .. +31, i.e.
-//                rows of the tile), adds any stream-K partials and C in fp32, rounds
+//                rows of the tile), adds any partial sums and C in fp32, rounds
 //                once to fp16 / bf16, writes the 32-row chunk to a swizzled
 //                shared-memory staging buffer and TMA-stores it (the store clips
 //                rows / columns outside D); then releases the accumulator on the
@@ -119,10 +122,6 @@ struct Params {
     // CTA a share of the tile's 32-row chunks, the partials in rank order), add C,
     // round once and store.  No global scratch is involved.
     int split;
-    // L2 prefetch distance of the B issuer, in k-blocks (0 = off): for problems bound by
-    // streaming B from memory, each B box is also requested into L2 this many k-blocks
-    // ahead of its load into shared memory.
-    int b_prefetch;
 };
 
 // How the block-scaled kinds move their scale factors (Config::SF_MODE).
@@ -616,8 +615,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // The set-up above touched only this CTA's own shared memory, TMEM and parameters,
     // so it may overlap the end of the previous launch on the stream (launched with
     // programmatic stream serialization).  Global memory is touched only after the
-    // previous grid has completed; the next launch may start its own set-up now.
-    griddep_wait();
+    // previous grid has completed: each thread that reads or writes it waits for that
+    // (griddep_wait) right before its first access, so that the roles' own set-up --
+    // the first tile's coordinates, the code and parameters it fetches, ~1600 cycles
+    // on a cold SM -- also overlaps the previous launch.  The next launch may start
+    // its own set-up now.
     griddep_launch_dependents();
 
     // ------------------------------------------------------------------ TMA issuers
@@ -634,6 +636,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         seg_begin(p, cluster, num_clusters, it);
         int tile, k0, k1, kind;
         bool first_seg = true;
+        bool dep_done = false;
         while (ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
             int mb, nb;
             tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
@@ -656,6 +659,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     continue;
                 }
 #endif
+                if (!dep_done) {  // first global access of this thread
+                    griddep_wait();
+                    dep_done = true;
+                }
                 const int kx = kb * Cfg::kKCoordPerStage;
                 const uint32_t dst =
                     role == 0 ? sbase + Cfg::OFF_A + s * Cfg::A_BYTES : sbase + Cfg::OFF_B + s * Cfg::B_BYTES;
@@ -668,14 +675,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
                     tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
-                }
-                if (role == 1 && p.b_prefetch > 0) {
-                    // the first k-blocks of the segment are requested at its start
-                    if (kb == k0)
-                        for (int f = k0 + 1; f < k1 && f <= k0 + p.b_prefetch; ++f)
-                            tma_prefetch_l2_2d(&tmB, f * Cfg::kKCoordPerStage, n0);
-                    if (kb + p.b_prefetch + 1 < k1)
-                        tma_prefetch_l2_2d(&tmB, (kb + p.b_prefetch + 1) * Cfg::kKCoordPerStage, n0);
                 }
                 ++loads[s];
                 if (++s == STAGES) {
@@ -728,6 +727,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             SegIter it;
             seg_begin(p, cluster, num_clusters, it);
             int tile, k0, k1, kind;
+            bool dep_done = false;
             while (ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
                 int mb, nb;
                 tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
@@ -742,6 +742,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (!wait_bar(free_bar, ph ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
+                    }
+                    if (!dep_done) {  // first global access of this thread
+                        griddep_wait();
+                        dep_done = true;
                     }
                     const int x = Cfg::kStageSlots ? (KIND == KIND_NVFP4 ? g : (g >> 2)) * 16 : g * Cfg::SF_W;
                     const uint32_t sb = bar(Cfg::BAR_SFFULL + r);
@@ -1054,6 +1058,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     };
     auto epilogue_role = [&]() {
         // -------------------------------------------------------------- epilogue
+        griddep_wait();  // C loads and D stores below
         constexpr int EC = Cfg::EPI_COLS;
         constexpr int EB = Cfg::EPI_BUFS;
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
