@@ -66,6 +66,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace tn {
@@ -437,18 +439,17 @@ __device__ __forceinline__ void load_chunk(uint32_t tacc, int c, uint32_t* r) {
         tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(c + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
 }
 
-// One thread's share of an epilogue chunk: output row `row`, columns n .. n+COLS-1
-// of the tile, accumulator words r[0..COLS-1].  With kCStaged the warp's staging
-// buffer already holds the matching C chunk (TMA-loaded with the D tensor map's
-// swizzle; zero outside C); the thread adds its row of it in fp32, rounds once and
-// writes the result back in place: 16-byte chunk j of row l lives at chunk
-// j ^ f(l), the XOR swizzle the D tensor map uses.
-template <int KIND, int COLS, bool kCStaged>
-__device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int lane) {
-    constexpr int VECS = COLS / 8;  // 16-byte output vectors per row
+// One thread's share of an epilogue chunk: output row `lane` of a 32-row x COLS
+// chunk, 16-byte output vectors v0 .. v0+NV-1 (8 values each) from the accumulator
+// words r[8v .. 8v+7].  With kCStaged the staging buffer already holds the matching
+// C chunk (TMA-loaded with the D tensor map's swizzle; zero outside C); the thread
+// adds its values in fp32, rounds once and writes the result back in place: 16-byte
+// vector j of row l lives at vector j ^ f(l), the XOR swizzle the D tensor map uses.
+template <int KIND, int COLS, int NV, bool kCStaged>
+__device__ __forceinline__ void stage_vectors(const uint32_t* r, uint8_t* buf, int lane, int v0) {
 #pragma unroll
-    for (int v = 0; v < VECS; ++v) {
-        uint4* slot = reinterpret_cast<uint4*>(buf + layout::swizzled_offset(COLS * 2, lane, 16 * v));
+    for (int v = 0; v < NV; ++v) {
+        uint4* slot = reinterpret_cast<uint4*>(buf + layout::swizzled_offset(COLS * 2, lane, 16 * (v0 + v)));
         float f[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
@@ -460,6 +461,12 @@ __device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int
         }
         *slot = pack8<KIND>(f);
     }
+}
+
+// The whole row: columns 0 .. COLS-1 of the chunk from r[0 .. COLS-1].
+template <int KIND, int COLS, bool kCStaged>
+__device__ __forceinline__ void stage_chunk(const uint32_t* r, uint8_t* buf, int lane) {
+    stage_vectors<KIND, COLS, COLS / 8, kCStaged>(r, buf, lane, 0);
 }
 
 // Scale-factor writer for one TMEM lane quarter.  The k-block's scales sit in a scale
@@ -637,6 +644,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int tile, k0, k1, kind;
         bool first_seg = true;
         bool dep_done = false;
+        // L2 policy of the boxes: an A panel serves every tile of its m block, so it is
+        // kept (evict_last); with a single row of tiles each B panel is read once, so it
+        // goes first.  Otherwise B is left to the default policy.
+        const bool hinted = role == 0 || p.num_m_blocks == 1;
+        const uint64_t policy = role == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
         while (ok && seg_next<Cfg::kStreamK, Cfg::kSplit>(p, num_clusters, it, tile, k0, k1, kind)) {
             int mb, nb;
             tile_coords(tile, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
@@ -671,10 +683,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t bytes = PAIR * (role == 0 ? Cfg::A_BYTES : Cfg::B_BYTES);
                 if constexpr (kPair) {
                     if (leader) mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
-                    tma_load_2d_pair(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y);
+                    if (hinted)
+                        tma_load_2d_pair_hint(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y, policy);
+                    else
+                        tma_load_2d_pair(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y);
                 } else {
                     mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
-                    tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
+                    if (hinted)
+                        tma_load_2d_hint(dst, map, bar(Cfg::BAR_FULL + s), kx, y, policy);
+                    else
+                        tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
                 }
                 ++loads[s];
                 if (++s == STAGES) {
@@ -1059,6 +1077,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     auto epilogue_role = [&]() {
         // -------------------------------------------------------------- epilogue
         griddep_wait();  // C loads and D stores below
+        const uint64_t out_policy = l2_policy_evict_first();  // C and D are touched once
         constexpr int EC = Cfg::EPI_COLS;
         constexpr int EB = Cfg::EPI_BUFS;
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
@@ -1077,7 +1096,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         auto load_c = [&](int b, int nc, int m_warp) {
             const uint32_t cb = bar(Cfg::BAR_CLOAD + e * EB + b);
             mbar_arrive_expect_tx(cb, Cfg::EPI_BUF_BYTES);
-            tma_load_2d(stg_u32 + b * Cfg::EPI_BUF_BYTES, &tmC, cb, nc, m_warp);
+            tma_load_2d_hint(stg_u32 + b * Cfg::EPI_BUF_BYTES, &tmC, cb, nc, m_warp, out_policy);
             cpending |= 1u << b;
         };
         bool ok = true;
@@ -1224,7 +1243,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) {
                         for (int c = c_begin, b = 0; c < c_end && n0 + c < p.N; c += EC, ++b)
-                            tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
+                            tma_store_2d_hint(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, n0 + c, m_warp, out_policy);
                         bulk_commit_group();
                     }
                 }
@@ -1272,7 +1291,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tmD, stg_u32, n0 + c, m_warp);
+                            tma_store_2d_hint(&tmD, stg_u32, n0 + c, m_warp, out_policy);
                             bulk_commit_group();
                         }
                     }
@@ -1308,7 +1327,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmD, stg_u32 + eb * Cfg::EPI_BUF_BYTES, n0 + c, m_warp);
+                        tma_store_2d_hint(&tmD, stg_u32 + eb * Cfg::EPI_BUF_BYTES, n0 + c, m_warp, out_policy);
                         bulk_commit_group();
                         if (has_c && EB == 1 && more) {
                             bulk_wait_group_read<0>();
@@ -1383,78 +1402,107 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
         }
     };
-    // split_reduce (after every slot has landed): the CTA's owned chunks are dealt to its
-    // epilogue warps; each adds the chunk's S slots in rank order, adds C, rounds once,
-    // stages and stores.
+    // split_reduce (after every slot has landed), by every warp of the CTA with a staging
+    // buffer: the CTA's owned chunks are cut into P column parts (P = 1, 2 or 4, as many
+    // as the warps allow), part j of owned chunk k going to warp kP + j.  Each warp adds
+    // its columns of the chunk's S slots in rank order, adds C, rounds once and stages
+    // them into the group's buffer; once the P warps of a group have staged (a named
+    // barrier), the group's first warp stores the chunk.  With P = 1 each warp takes
+    // whole chunks, round robin.
     auto split_reduce = [&]() {
         if constexpr (Cfg::kSplit) {
             constexpr int EC = Cfg::EPI_COLS;
-            constexpr int EB = Cfg::EPI_BUFS;
             constexpr int UNITS = 4 * (BN / EC);
-            const int e = warp - 4;
+            constexpr int NBUF = Cfg::EPI_WARPS * Cfg::EPI_BUFS;  // staging buffers, one C barrier each
+            constexpr int NW = (Cfg::THREADS / 32) < NBUF ? (Cfg::THREADS / 32) : NBUF;
+            static_assert(NW % 4 == 0, "groups of up to four warps");
+            if (warp >= NW) return;
+            griddep_wait();  // C loads and D stores (returns at once: the previous grid is done)
+            const uint64_t out_policy = l2_policy_evict_first();
             const int S = p.split;
             const int r = static_cast<int>(blockIdx.x) % S;
+            const int owned = (UNITS - r + S - 1) / S;  // chunks u = r + kS < UNITS
             int mb, nb;
             tile_coords(static_cast<int>(blockIdx.x) / S, p.num_m_blocks, p.num_n_blocks, p.raster_group, mb, nb);
-            uint8_t* stg = smem + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
-            const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + e * (EB * Cfg::EPI_BUF_BYTES);
             const bool has_c = p.C != nullptr;
-            uint32_t cph = 0, cpending = 0;
-            bool ok = *abort_flag == 0;
-            int j = 0;
-            for (int k = e, u = r + e * S; ok && u < UNITS; k += 4, u += 4 * S) {
-                const int q = u & 3, g = u >> 2;
-                const int m_warp = mb * Cfg::BM + q * 32;
-                const int nc = nb * BN + g * EC;
-                if (m_warp >= p.M || nc >= p.N) continue;  // warp-uniform
-                const int b = j % EB;
-                ++j;
-                const uint32_t cb = bar(Cfg::BAR_CLOAD + e * EB + b);
-                if (lane == 0) {
-                    bulk_wait_group_read<EB - 1>();  // buffer b's previous store has read it
+            auto run = [&](auto parts) {
+                constexpr int P = decltype(parts)::value;
+                constexpr int W = EC / P;  // columns of a part
+                static_assert(W % 8 == 0, "whole 16-byte output vectors");
+                const int grp = warp / P, part = warp % P;
+                const bool first = part == 0 && lane == 0;  // issues the group's copies
+                uint8_t* stg = smem + Cfg::OFF_EPI + grp * Cfg::EPI_BUF_BYTES;
+                const uint32_t stg_u32 = sbase + Cfg::OFF_EPI + grp * Cfg::EPI_BUF_BYTES;
+                const uint32_t cb = bar(Cfg::BAR_CLOAD + grp);
+                uint32_t cph = 0;
+                bool ok = *abort_flag == 0;
+                // P > 1: owned * P <= NW, one round; P = 1: warp w takes chunks w, w + NW, ...
+                for (int k = grp; ok && k < owned; k += NW / P) {
+                    const int u = r + k * S;
+                    const int q = u & 3, g = u >> 2;
+                    const int m_warp = mb * Cfg::BM + q * 32;
+                    const int nc = nb * BN + g * EC;
+                    if (m_warp >= p.M || nc >= p.N) continue;  // uniform over the group
+                    if (first) {
+                        bulk_wait_group_read<0>();  // P = 1: the buffer's previous store has read it
+                        if (has_c) {
+                            mbar_arrive_expect_tx(cb, Cfg::EPI_BUF_BYTES);
+                            tma_load_2d_hint(stg_u32, &tmC, cb, nc, m_warp, out_policy);
+                        }
+                    }
+                    __syncwarp();
+                    uint32_t acc[W];
+#pragma unroll
+                    for (int i = 0; i < W; ++i) acc[i] = 0u;  // +0.0f
+                    const float4* slot =
+                        reinterpret_cast<const float4*>(smem + Cfg::OFF_A + k * S * UNIT_BYTES) + part * (W / 4) * 32 + lane;
+                    for (int src = 0; src < S; ++src, slot += UNIT_BYTES / 16) {
+#pragma unroll
+                        for (int i = 0; i < W / 4; ++i) {
+                            const float4 v = slot[i * 32];
+                            acc[4 * i] = __float_as_uint(__uint_as_float(acc[4 * i]) + v.x);
+                            acc[4 * i + 1] = __float_as_uint(__uint_as_float(acc[4 * i + 1]) + v.y);
+                            acc[4 * i + 2] = __float_as_uint(__uint_as_float(acc[4 * i + 2]) + v.z);
+                            acc[4 * i + 3] = __float_as_uint(__uint_as_float(acc[4 * i + 3]) + v.w);
+                        }
+                    }
                     if (has_c) {
-                        mbar_arrive_expect_tx(cb, Cfg::EPI_BUF_BYTES);
-                        tma_load_2d(stg_u32 + b * Cfg::EPI_BUF_BYTES, &tmC, cb, nc, m_warp);
+                        if constexpr (P == 1) {
+                            ok = __all_sync(0xffffffffu, wait_bar(cb, cph, abort_flag, p.err));
+                            if (!ok) {
+                                if (first) wait_bar_drain(cb, cph);  // the C load lands before the CTA exits
+                                break;
+                            }
+                        } else {
+                            // every warp of the group must reach the named barrier below:
+                            // a bounded wait that does not give up on the abort flag
+                            wait_bar_drain(cb, cph);
+                            __syncwarp();
+                        }
+                        cph ^= 1u;
+                        stage_vectors<KIND, EC, W / 8, true>(acc, stg, lane, part * (W / 8));
+                    } else {
+                        stage_vectors<KIND, EC, W / 8, false>(acc, stg, lane, part * (W / 8));
+                    }
+                    fence_proxy_async_smem();
+                    if constexpr (P > 1)
+                        named_bar_sync(1 + grp, 32 * P);
+                    else
+                        __syncwarp();
+                    if (first && *abort_flag == 0) {
+                        tma_store_2d_hint(&tmD, stg_u32, nc, m_warp, out_policy);
+                        bulk_commit_group();
                     }
                 }
-                if (has_c) cpending |= 1u << b;
+                if (first) bulk_wait_group_all();
                 __syncwarp();
-                uint32_t acc[EC];
-#pragma unroll
-                for (int i = 0; i < EC; ++i) acc[i] = 0u;  // +0.0f
-                const float4* slot = reinterpret_cast<const float4*>(smem + Cfg::OFF_A + k * S * UNIT_BYTES) + lane;
-                for (int src = 0; src < S; ++src, slot += UNIT_BYTES / 16) {
-#pragma unroll
-                    for (int i = 0; i < EC / 4; ++i) {
-                        const float4 v = slot[i * 32];
-                        acc[4 * i] = __float_as_uint(__uint_as_float(acc[4 * i]) + v.x);
-                        acc[4 * i + 1] = __float_as_uint(__uint_as_float(acc[4 * i + 1]) + v.y);
-                        acc[4 * i + 2] = __float_as_uint(__uint_as_float(acc[4 * i + 2]) + v.z);
-                        acc[4 * i + 3] = __float_as_uint(__uint_as_float(acc[4 * i + 3]) + v.w);
-                    }
-                }
-                if (has_c) {
-                    ok = __all_sync(0xffffffffu, wait_bar(cb, (cph >> b) & 1u, abort_flag, p.err));
-                    cph ^= 1u << b;
-                    cpending &= ~(1u << b);
-                    if (!ok) break;
-                    stage_chunk<KIND, EC, true>(acc, stg + b * Cfg::EPI_BUF_BYTES, lane);
-                } else {
-                    stage_chunk<KIND, EC, false>(acc, stg + b * Cfg::EPI_BUF_BYTES, lane);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmD, stg_u32 + b * Cfg::EPI_BUF_BYTES, nc, m_warp);
-                    bulk_commit_group();
-                }
-            }
-            if (lane == 0) {
-                for (int b = 0; b < EB; ++b)
-                    if (cpending & (1u << b)) wait_bar_drain(bar(Cfg::BAR_CLOAD + e * EB + b), (cph >> b) & 1u);
-                bulk_wait_group_all();
-            }
-            __syncwarp();
+            };
+            if (4 * owned <= NW)
+                run(std::integral_constant<int, 4>{});
+            else if (2 * owned <= NW)
+                run(std::integral_constant<int, 2>{});
+            else
+                run(std::integral_constant<int, 1>{});
         }
     };
 
@@ -1501,7 +1549,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (*abort_flag == 0) split_push();
             __syncwarp();
             cluster_sync_all();
-            if (warp >= 4 && warp < 8) split_reduce();
+            split_reduce();
             __syncwarp();
         }
     }
