@@ -199,7 +199,7 @@ __device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it
 
 template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
           int EPI_WARPS_ = 4, int ROW_BYTES_ = 128, bool REG_DRAIN_ = false, int SF_MODE_ = 0, int SF_W_ = 16,
-          int SF_SLOTS_ = 2, bool DIRECT_STORE_ = false>
+          int SF_SLOTS_ = 2>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
@@ -229,15 +229,6 @@ struct Config {
     // Staging covers a warp's whole 32-row slice of the tile: the accumulator is
     // drained to shared memory and released before any store is issued.
     static constexpr bool kWholeTileStaging = EPI_COLS * EPI_BUFS == BN / EPI_SPLIT;
-    // Direct stores (small tiles, where the epilogue's latency is the launch's tail):
-    // each epilogue thread takes its row of the warp's slice into registers, releases
-    // the accumulator and writes its 16-byte output vectors straight to D (C read the
-    // same way, fetched before the accumulator is ready) -- no staging, proxy fence,
-    // TMA store or store wait.  Whole tiles; a cluster split still reduces through
-    // the staging buffers.
-    static constexpr bool kDirectStore = DIRECT_STORE_;
-    static_assert(!kDirectStore || (kWholeTileStaging && EPI_BUFS == 1 && PAIR == 1 && BN <= 64),
-                  "direct stores: one staged chunk of at most 64 columns per warp");
     // Register drain (block-scaled pairs, 8 epilogue warps, 512 threads = 4 warpgroups):
     // the issuers / MMA warpgroup and the scale writers give up registers
     // (setmaxnreg) so that each epilogue warp takes its whole 32 x 128 slice of the
@@ -1195,18 +1186,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             };
             // C does not depend on the accumulator: fetch it early
-            const int row = m_warp + lane;  // this thread's output row (direct stores)
-            uint4 cdir[Cfg::kDirectStore ? Cfg::BN_EPI / 8 : 1];
-            if constexpr (Cfg::kDirectStore) {
-#pragma unroll
-                for (int v = 0; v < Cfg::BN_EPI / 8; ++v) {
-                    const int col = n0 + c_begin + 8 * v;
-                    cdir[v] = make_uint4(0u, 0u, 0u, 0u);
-                    if (has_c && row < p.M && col < p.N)
-                        cdir[v] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.C) +
-                                                                        static_cast<size_t>(row) * p.N + col));
-                }
-            } else if constexpr (Cfg::kWholeTileStaging) {
+            if constexpr (Cfg::kWholeTileStaging) {
                 if (rows_in && lane == 0) {
                     bulk_wait_group_read<0>();  // the previous tile's stores have read the buffers
                     if (has_c)
@@ -1227,35 +1207,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
-            if constexpr (Cfg::kDirectStore) {
-                uint32_t r[Cfg::BN_EPI];
-                load_chunk<Cfg::BN_EPI>(tacc, c_begin, r);
-                tmem_ld_wait();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(Cfg::BAR_TEMPTY + buf));
-                if constexpr (kSK) {
-                    if (rows_in) add_partials(r, 0);
-                }
-                if (row < p.M) {
-#pragma unroll
-                    for (int v = 0; v < Cfg::BN_EPI / 8; ++v) {
-                        const int col = n0 + c_begin + 8 * v;
-                        if (col >= p.N) break;
-                        float f[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) f[i] = acc_value<KIND>(r[8 * v + i]);
-                        if (has_c) {
-                            float c[8];
-                            unpack8<KIND>(cdir[v], c);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) f[i] += c[i];
-                        }
-                        __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.D) + static_cast<size_t>(row) * p.N + col),
-                               pack8<KIND>(f));
-                    }
-                }
-            } else if constexpr (Cfg::kWholeTileStaging) {
+            if constexpr (Cfg::kWholeTileStaging) {
                 // Drain every chunk into its own staging buffer, release the
                 // accumulator, then store: the MMAs of the next tile wait only for
                 // the TMEM reads.
