@@ -140,3 +140,30 @@ def sample_rows(M: int, n: int, seed: int = 0) -> list:
     fixed = [r for r in fixed if 0 <= r < M]
     extra = rng.choice(M, size=min(M, max(0, n - len(fixed))), replace=False).tolist()
     return sorted(set(fixed + extra))
+
+
+_DRIVER = {}
+
+
+def dispatch_plan(M: int, N: int, K: int, kpb: int, sms: int) -> list:
+    """The host-side dispatch rules' choices for one problem, from the dispatch driver
+    (tests/dispatch_driver.cpp, built once per process with the host compiler):
+    [fixed-scratch instance, stream-K flag, block-scaled pair, dense plan instance,
+    dense plan split, block-scaled split, raster group]."""
+    import os
+    import shutil
+    import subprocess
+    import tempfile
+    import pytest
+    if "exe" not in _DRIVER:
+        cxx = shutil.which("g++") or shutil.which("c++")
+        if cxx is None:
+            pytest.skip("no host C++ compiler")
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        exe = os.path.join(tempfile.mkdtemp(prefix="dispatch"), "dispatch_driver")
+        subprocess.run([cxx, "-std=c++17", "-O1", "-I", os.path.join(root, "cute_layouts_mma_gb300", "csrc"),
+                        os.path.join(root, "tests", "dispatch_driver.cpp"), "-o", exe], check=True)
+        _DRIVER["exe"] = exe
+    out = subprocess.run([_DRIVER["exe"], str(sms), str(M), str(N), str(K), str(kpb)], check=True,
+                         capture_output=True, text=True).stdout.split()
+    return [int(v) for v in out]

@@ -251,6 +251,23 @@ def test_split_fp16_integers_bit_exact(M, N, K, with_c):
     P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 24, seed=1), mode="exact")
 
 
+# The reduction cuts each CTA's owned chunks into 1, 2 or 4 column parts, as the
+# cluster size leaves room: clusters of 3 (6 or 5 owned 32 x 64 chunks of a 128 x 256
+# tile: whole chunks per warp), 6 (3 or 2: halves), 8 (2: quarters) and, on 128 x 128
+# tiles, 8 (1: quarters, half the warps idle).  The expected cluster sizes are the
+# dispatch rules' on a 152-SM device.
+@pytest.mark.parametrize("M,N,K,split", [(512, 2560, 8192, 3), (256, 2560, 16384, 6), (128, 4096, 4096, 8),
+                                         (200, 1000, 32768, 8)])
+def test_split_reduce_parts_fp16_integers_bit_exact(M, N, K, split):
+    sms = torch.cuda.get_device_properties(P.device()).multi_processor_count
+    plan = P.dispatch_plan(M, N, K, 64, sms)
+    assert plan[4] > 1, "the shape no longer takes a cluster split"
+    if sms == 152:
+        assert plan[4] == split
+    prob = inputs.make_problem("f16", M, N, K, seed=M + 7 * N + K, dist="int2", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 32, seed=7), mode="exact")
+
+
 def test_split_fp16_in_place():
     prob = inputs.make_problem("f16", 300, 520, 16384, seed=21, dist="int2", with_c=True)
     g = P.to_device(prob, P.device())

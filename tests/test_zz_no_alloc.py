@@ -22,9 +22,6 @@ This file sorts last so that it also runs after every other GPU test; it needs
 no state from them and passes alone in a fresh process as well.
 """
 import ctypes
-import os
-import shutil
-import subprocess
 
 import numpy as np
 import pytest
@@ -36,8 +33,6 @@ from cute_layouts_mma_gb300 import inputs
 import _parity as P
 
 pytestmark = pytest.mark.gpu
-
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _noalloc(g, D, stream):
@@ -58,31 +53,17 @@ def _f16(g, D, stream):
                              ctypes.c_void_p(stream.cuda_stream))
 
 
-def _stream_k_choice(M, N, K, sms, tmp_path):
-    """(dense instance, stream-K split flag) of the fixed-scratch call's rule, from the
-    host-side dispatch driver built with the host compiler."""
-    cxx = shutil.which("g++") or shutil.which("c++")
-    if cxx is None:
-        pytest.skip("no host C++ compiler")
-    exe = str(tmp_path / "dispatch_driver")
-    subprocess.run([cxx, "-std=c++17", "-O1", "-I", os.path.join(ROOT, "cute_layouts_mma_gb300", "csrc"),
-                    os.path.join(ROOT, "tests", "dispatch_driver.cpp"), "-o", exe], check=True)
-    out = subprocess.run([exe, str(sms), str(M), str(N), str(K), "64"], check=True, capture_output=True,
-                         text=True).stdout.split()
-    return int(out[0]), int(out[1])
-
-
 # 128 x 2560 x 16384 on the fixed-scratch call: the 128 x 256 tiles would split, so it
 # takes the 128 x 128 single-CTA instance (20 tiles) with the stream-K schedule.
 SPLIT_SHAPE = (128, 2560, 16384)
 
 
-def test_noalloc_stream_k_integers_bit_exact_twice(tmp_path):
+def test_noalloc_stream_k_integers_bit_exact_twice():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     dev = P.device()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    choice, split = _stream_k_choice(*SPLIT_SHAPE, sms, tmp_path)
+    choice, split = P.dispatch_plan(*SPLIT_SHAPE, 64, sms)[:2]
     assert (choice, split) == (2, 1), "the shape no longer takes the stream-K schedule on this device"
     stream = torch.cuda.current_stream(dev)
     M, N, K = SPLIT_SHAPE
