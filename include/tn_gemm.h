@@ -39,6 +39,11 @@
  *     and returns; gemm_last_device_error() reports it.
  *   - Calls may be made from several host threads; the library's only state is
  *     per-device, set up on first use (kernel attributes, SM count).
+ *   - The kernels' copies carry L2 eviction hints, which change no result: A is
+ *     kept in L2 ahead of other lines (it is reused by every tile of its rows), C
+ *     and D are read or written once and let go first, and so is B when the
+ *     output has a single row of tiles.  A D that the next kernel reads at once
+ *     may therefore come from DRAM rather than L2.
  *
  * Numerics: products are formed by the tensor cores
  * and summed in fp32 (GEMM_ACC_F32) or fp16 (GEMM_ACC_F16); C is added in fp32
