@@ -237,6 +237,18 @@ def test_mxfp8_128x16384_full_size_sampled_rows():
     assert torch.isfinite(D.float()).all()
 
 
+def test_fp16_pairs_partial_backward_raster_group():
+    # 21 rows of 256 x 256 pair tiles run as raster groups of 16 and 5 m blocks; the
+    # second (odd) group sweeps the columns backwards and is cut short
+    M, N, K = 5376, 1024, 256
+    sms = torch.cuda.get_device_properties(P.device()).multi_processor_count
+    plan = P.dispatch_plan(M, N, K, 64, sms)
+    assert plan[3] == 0 and plan[6] == 16, "not a CTA-pair launch with raster groups of 16"
+    prob = inputs.make_problem("f16", M, N, K, seed=61, dist="int2", with_c=True)
+    rows = [0, 255, 4095, 4096, 4100, 4351, 4352, 5000, 5375] + P.sample_rows(M, 16, seed=8)
+    P.check(prob, P.run_gpu(prob, accum=0), rows=sorted(set(rows)), mode="exact")
+
+
 # ------------------------------------------------------------------ split schedules
 # Skinny shapes with long K, whose whole tiles would leave most of the device idle:
 # the fp32 kinds give each tile to a cluster of up to 8 CTAs that split its k-blocks
