@@ -19,10 +19,11 @@ using CfgE5m2 = Config<KIND_FP8_E5M2, 256, 4, 2, 64, 2, 1>;
 using CfgBf16N128 = Config<KIND_BF16, 128, 6, 2, 64, 2, 1>;
 using CfgE4m3N128 = Config<KIND_FP8_E4M3, 128, 6, 2, 64, 2, 1>;
 using CfgE5m2N128 = Config<KIND_FP8_E5M2, 128, 6, 2, 64, 2, 1>;
-// Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs.
-using CfgBf16N64 = Config<KIND_BF16, 64, 4, 2, 64, 1, 1>;
-using CfgE4m3N64 = Config<KIND_FP8_E4M3, 64, 4, 2, 64, 1, 1>;
-using CfgE5m2N64 = Config<KIND_FP8_E5M2, 64, 4, 2, 64, 1, 1>;
+// Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, two boxes of K
+// per stage (as FP16).
+using CfgBf16N64 = Config<KIND_BF16, 64, 4, 2, 64, 1, 1, 4, 128, false, 0, 16, 2, 2>;
+using CfgE4m3N64 = Config<KIND_FP8_E4M3, 64, 4, 2, 64, 1, 1, 4, 128, false, 0, 16, 2, 2>;
+using CfgE5m2N64 = Config<KIND_FP8_E5M2, 64, 4, 2, 64, 1, 1, 4, 128, false, 0, 16, 2, 2>;
 
 // Device-side record of an abandoned launch (a bounded wait ran out).
 static __device__ unsigned int g_err_dense;
@@ -42,8 +43,8 @@ gemm_status_t run(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
     CUtensorMap ta, tb, td, tc;
     // A [M][K], 128-row boxes; B [N][K], BN/PAIR-row boxes; 128 bytes of K per box
     // (64 BF16 or 128 FP8 elements).  D, C: bf16 [M][N] in 32-row x EPI_COLS boxes.
-    if (!encode_tma_2d(&ta, in_type, A, K, M, row_bytes, Cfg::kKCoordPerStage, Cfg::BM, 128) ||
-        !encode_tma_2d(&tb, in_type, B, K, N, row_bytes, Cfg::kKCoordPerStage, Cfg::BN_CTA, 128) ||
+    if (!encode_tma_2d(&ta, in_type, A, K, M, row_bytes, Cfg::kKBoxCoord, Cfg::BM, 128) ||
+        !encode_tma_2d(&tb, in_type, B, K, N, row_bytes, Cfg::kKBoxCoord, Cfg::BN_CTA, 128) ||
         !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
                        Cfg::EPI_ROW_BYTES))
         return GEMM_ERR_CUDA;

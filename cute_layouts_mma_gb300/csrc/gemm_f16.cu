@@ -15,9 +15,11 @@ using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
 // Skinny problems (fp32 accumulation): 128-column tiles where they move fewer bytes
 // per SM than 128 x 256 ones (each instance with its own cluster split).
 using CfgF16N128 = Config<KIND_F16_ACC32, 128, 6, 2, 64, 2, 1>;
-// Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages, each
-// epilogue warp staging its whole 32 x 64 slice.
-using CfgF16N64 = Config<KIND_F16_ACC32, 64, 4, 2, 64, 1, 1>;
+// Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages of two
+// 128-byte boxes of K per operand row (8 MMAs per barrier wait and commit: an N = 64 MMA is
+// short, and with one box per stage the MMA thread's per-stage work bounded these launches),
+// each epilogue warp staging its whole 32 x 64 slice.
+using CfgF16N64 = Config<KIND_F16_ACC32, 64, 4, 2, 64, 1, 1, 4, 128, false, 0, 16, 2, 2>;
 // Narrow K (fp32 accumulation): a whole K of at most 32 or 16 elements fits a 64- or
 // 32-byte operand row, stored with the 64- or 32-byte swizzle; 2 or 1 MMAs per stage
 // instead of 4 over zero-filled K.  These launches are bound by the C and D traffic,
@@ -51,7 +53,7 @@ gemm_status_t prepare(int64_t M, int64_t N, int64_t K, const void* A, const void
     // A: fp16 [M][K], 128-row boxes; B: fp16 [N][K], BN/PAIR-row boxes; kRowBytes
     // (128, or 64 / 32 for narrow K) of K per box, swizzled to match.  D: fp16 [M][N],
     // stored in 32-row x EPI_COLS boxes.
-    constexpr int kKBox = Cfg::kKCoordPerStage, kSw = Cfg::kRowBytes;
+    constexpr int kKBox = Cfg::kKBoxCoord, kSw = Cfg::kRowBytes;
     if (!encode_tma_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, K * 2, kKBox, Cfg::BM, kSw) ||
         !encode_tma_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, K * 2, kKBox, Cfg::BN_CTA, kSw) ||
         !encode_tma_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, N, M, N * 2, Cfg::EPI_COLS, 32,
@@ -69,7 +71,7 @@ gemm_status_t prepare(int64_t M, int64_t N, int64_t K, const void* A, const void
     p.K = static_cast<int>(K);
     p.num_m_blocks = static_cast<int>((M + Cfg::BM_TILE - 1) / Cfg::BM_TILE);
     p.num_n_blocks = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
-    p.num_k_blocks = static_cast<int>((K + kKBox - 1) / kKBox);
+    p.num_k_blocks = static_cast<int>((K + Cfg::kKCoordPerStage - 1) / Cfg::kKCoordPerStage);  // stages
     p.C = C;
     p.D = D;
     p.err = err;

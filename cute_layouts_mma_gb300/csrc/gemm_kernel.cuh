@@ -199,7 +199,7 @@ __device__ __forceinline__ bool seg_next(const Params& p, int units, SegIter& it
 
 template <int KIND_, int BN_, int STAGES_, int ACC_BUFS_, int EPI_COLS_, int EPI_BUFS_, int PAIR_,
           int EPI_WARPS_ = 4, int ROW_BYTES_ = 128, bool REG_DRAIN_ = false, int SF_MODE_ = 0, int SF_W_ = 16,
-          int SF_SLOTS_ = 2>
+          int SF_SLOTS_ = 2, int KSUB_ = 1>
 struct Config {
     static constexpr int KIND = KIND_;
     static constexpr int PAIR = PAIR_;  // CTAs per MMA (cta_group)
@@ -253,12 +253,21 @@ struct Config {
     static constexpr int kRowBytes = ROW_BYTES_;
     static_assert(kRowBytes == 128 || kRowBytes == 64 || kRowBytes == 32, "128-, 64- or 32-byte operand rows");
     static_assert(kRowBytes == 128 || is_dense(KIND_), "block-scaled stages hold 128 bytes of K");
-    static constexpr int kMmasPerStage = kRowBytes / 32;
+    // A stage holds kSub boxes of kRowBytes of K per operand row (dense kinds only):
+    // kSub = 2 halves the MMA thread's barrier wait and commit per MMA, for tiles whose
+    // MMAs are short (N = 64).
+    static constexpr int kSub = KSUB_;
+    static_assert(kSub == 1 || (kSub == 2 && is_dense(KIND_) && ROW_BYTES_ == 128), "two boxes per stage: dense kinds");
+    static constexpr int kMmasPerSub = kRowBytes / 32;
+    static constexpr int kMmasPerStage = kSub * kMmasPerSub;
     // Elements of K per 128-byte row slice, in TMA coordinates (NVFP4 maps are bytes).
-    static constexpr int kKCoordPerStage = operands_16bit(KIND) ? kRowBytes / 2 : kRowBytes;
+    static constexpr int kKBoxCoord = operands_16bit(KIND) ? kRowBytes / 2 : kRowBytes;  // K of one box
+    static constexpr int kKCoordPerStage = kSub * kKBoxCoord;
 
-    static constexpr int A_BYTES = BM * kRowBytes;
-    static constexpr int B_BYTES = BN_CTA * kRowBytes;
+    static constexpr int A_SUB = BM * kRowBytes;      // one box of A
+    static constexpr int B_SUB = BN_CTA * kRowBytes;  // one box of B
+    static constexpr int A_BYTES = kSub * A_SUB;
+    static constexpr int B_BYTES = kSub * B_SUB;
     static constexpr int SFB_TCOLS = kBlockScaled ? BN / 32 : 0;             // TMEM columns of a tile's SFB
     static_assert(!kBlockScaled || BN % 32 == 0, "block-scaled tiles of whole 32-row scale columns");
     // Scale ring (block-scaled): SF_SLOTS slots, each holding SF_W bytes of every scale
@@ -682,18 +691,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const CUtensorMap* map = role == 0 ? &tmA : &tmB;
                 const int y = role == 0 ? m0 : n0;
                 const uint32_t bytes = PAIR * (role == 0 ? Cfg::A_BYTES : Cfg::B_BYTES);
+                const uint32_t sub_bytes = role == 0 ? Cfg::A_SUB : Cfg::B_SUB;
                 if constexpr (kPair) {
                     if (leader) mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
-                    if (hinted)
-                        tma_load_2d_pair_hint(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y, policy);
-                    else
-                        tma_load_2d_pair(dst, map, leader_bar(Cfg::BAR_FULL + s), kx, y);
                 } else {
                     mbar_arrive_expect_tx(bar(Cfg::BAR_FULL + s), bytes);
-                    if (hinted)
-                        tma_load_2d_hint(dst, map, bar(Cfg::BAR_FULL + s), kx, y, policy);
-                    else
-                        tma_load_2d(dst, map, bar(Cfg::BAR_FULL + s), kx, y);
+                }
+#pragma unroll
+                for (int j = 0; j < Cfg::kSub; ++j) {
+                    const uint32_t dj = dst + j * sub_bytes;
+                    const int xj = kx + j * Cfg::kKBoxCoord;
+                    if constexpr (kPair) {
+                        if (hinted)
+                            tma_load_2d_pair_hint(dj, map, leader_bar(Cfg::BAR_FULL + s), xj, y, policy);
+                        else
+                            tma_load_2d_pair(dj, map, leader_bar(Cfg::BAR_FULL + s), xj, y);
+                    } else {
+                        if (hinted)
+                            tma_load_2d_hint(dj, map, bar(Cfg::BAR_FULL + s), xj, y, policy);
+                        else
+                            tma_load_2d(dj, map, bar(Cfg::BAR_FULL + s), xj, y);
+                    }
                 }
                 ++loads[s];
                 if (++s == STAGES) {
@@ -867,16 +885,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                         (KIND == KIND_BF16 || KIND == KIND_FP8_E5M2) ? 1u : 0u);
 #pragma unroll
                         for (int j = 0; j < Cfg::kMmasPerStage; ++j) {
+                            // box j / kMmasPerSub of the stage, 32-byte K step j % kMmasPerSub
+                            constexpr int kPerSub = Cfg::kMmasPerSub;
+                            const uint64_t da = adesc + static_cast<uint64_t>((j / kPerSub) * (Cfg::A_SUB >> 4) + 2 * (j % kPerSub));
+                            const uint64_t db = bdesc + static_cast<uint64_t>((j / kPerSub) * (Cfg::B_SUB >> 4) + 2 * (j % kPerSub));
                             if constexpr (operands_16bit(KIND)) {
                                 if constexpr (kPair)
-                                    mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                                    mma_f16_pair(d_tmem, da, db, idesc, acc_kb || j != 0);
                                 else
-                                    mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                                    mma_f16(d_tmem, da, db, idesc, acc_kb || j != 0);
                             } else {
                                 if constexpr (kPair)
-                                    mma_f8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                                    mma_f8f6f4_pair(d_tmem, da, db, idesc, acc_kb || j != 0);
                                 else
-                                    mma_f8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, acc_kb || j != 0);
+                                    mma_f8f6f4(d_tmem, da, db, idesc, acc_kb || j != 0);
                             }
                         }
                     } else {

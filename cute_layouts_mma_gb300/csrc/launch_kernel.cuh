@@ -160,7 +160,7 @@ cudaError_t split_capacity(int sms, int dev, int (&res)[dispatch::kMaxSplit + 1]
 // scales).
 template <class Cfg>
 int raster_for(const Params& p, int units) {
-    const long long row = static_cast<long long>(p.num_k_blocks) * Cfg::kRowBytes;
+    const long long row = static_cast<long long>(p.num_k_blocks) * Cfg::kRowBytes * Cfg::kSub;
     const long long sf = Cfg::KIND == KIND_NVFP4 ? row / 8 : Cfg::KIND == KIND_MXFP8 ? row / 32 : 0;
     return dispatch::raster_group(p.num_m_blocks, p.num_n_blocks, units, Cfg::BM_TILE * (row + sf),
                                   static_cast<long long>(Cfg::BN) * (row + sf));
