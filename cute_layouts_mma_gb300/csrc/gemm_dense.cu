@@ -15,10 +15,11 @@ using CfgE4m3Pair = Config<KIND_FP8_E4M3, 256, 6, 2, 64, 2, 2>;
 using CfgE4m3 = Config<KIND_FP8_E4M3, 256, 4, 2, 64, 2, 1>;
 using CfgE5m2Pair = Config<KIND_FP8_E5M2, 256, 6, 2, 64, 2, 2>;
 using CfgE5m2 = Config<KIND_FP8_E5M2, 256, 4, 2, 64, 2, 1>;
-// Skinny problems: 128-column tiles where they move fewer bytes per SM (as FP16).
-using CfgBf16N128 = Config<KIND_BF16, 128, 6, 2, 64, 2, 1>;
-using CfgE4m3N128 = Config<KIND_FP8_E4M3, 128, 6, 2, 64, 2, 1>;
-using CfgE5m2N128 = Config<KIND_FP8_E5M2, 128, 6, 2, 64, 2, 1>;
+// Skinny problems: 128-column tiles where they move fewer bytes per SM, 3 stages of two
+// boxes of K (as FP16).
+using CfgBf16N128 = Config<KIND_BF16, 128, 3, 2, 64, 2, 1, 4, 128, false, 0, 16, 2, 2>;
+using CfgE4m3N128 = Config<KIND_FP8_E4M3, 128, 3, 2, 64, 2, 1, 4, 128, false, 0, 16, 2, 2>;
+using CfgE5m2N128 = Config<KIND_FP8_E5M2, 128, 3, 2, 64, 2, 1, 4, 128, false, 0, 16, 2, 2>;
 // Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, two boxes of K
 // per stage (as FP16).
 using CfgBf16N64 = Config<KIND_BF16, 64, 4, 2, 64, 1, 1, 4, 128, false, 0, 16, 2, 2>;

@@ -13,8 +13,9 @@ using CfgF16Acc16Pair = Config<KIND_F16_ACC16, 256, 6, 2, 64, 2, 2>;
 using CfgF16Acc32 = Config<KIND_F16_ACC32, 256, 4, 2, 64, 2, 1>;
 using CfgF16Acc16 = Config<KIND_F16_ACC16, 256, 4, 2, 64, 2, 1>;
 // Skinny problems (fp32 accumulation): 128-column tiles where they move fewer bytes
-// per SM than 128 x 256 ones (each instance with its own cluster split).
-using CfgF16N128 = Config<KIND_F16_ACC32, 128, 6, 2, 64, 2, 1>;
+// per SM than 128 x 256 ones (each instance with its own cluster split); 3 stages of
+// two boxes of K (8 MMAs of N = 128 per barrier wait and commit).
+using CfgF16N128 = Config<KIND_F16_ACC32, 128, 3, 2, 64, 2, 1, 4, 128, false, 0, 16, 2, 2>;
 // Small problems (dispatch::use_small_tiles): 128 x 64 tiles on single CTAs, 4 stages of two
 // 128-byte boxes of K per operand row (8 MMAs per barrier wait and commit: an N = 64 MMA is
 // short, and with one box per stage the MMA thread's per-stage work bounded these launches),
