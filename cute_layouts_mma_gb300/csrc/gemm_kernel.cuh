@@ -21,10 +21,10 @@
 // halves the B bytes loaded from L2 and read by the tensor core.
 //
 // Warps of each CTA:
-//   warps 0, 2   TMA issuers for A and B: per K slice of kRowBytes (128, or 64 / 32
-//                for narrow K), load this CTA's A (warp 0) and B (warp 2) box into
-//                swizzled shared memory and
-//                arm the leader's `full` barrier with the bytes (PAIR = 2: the
+//   warps 0, 2   TMA issuers for A and B: per stage, load this CTA's A (warp 0) and
+//                B (warp 2) boxes of kRowBytes of K (128, or 64 / 32 for narrow K;
+//                kSub boxes one after the other along K) into swizzled shared memory
+//                and arm the leader's `full` barrier with the bytes (PAIR = 2: the
 //                peer's copies signal the leader's barrier directly).  A TMA
 //                instruction occupies its issuing warp for a few hundred cycles
 //                whatever the box size, so each operand stream has its own warp.
