@@ -400,13 +400,21 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 // Arrive on an mbarrier that may live in the peer CTA, without release semantics.
 // Used only where what is signalled is TMEM traffic, not generic memory: scale stores
 // completed by tcgen05.wait::st, or accumulator loads completed by tcgen05.wait::ld.
-// The PTX ISA orders tcgen05 operations of two threads through a thread
-// synchronization bracketed by tcgen05.fence::before_thread_sync in the signalling
-// thread (after its wait::st / wait::ld) and tcgen05.fence::after_thread_sync in the
-// waiting thread (before its tcgen05.mma); the mbarrier arrive / wait pair is that
-// synchronization, and its release / acquire semantics concern generic memory only
-// (memory consistency model: tcgen05 operations, and the mbarrier's .sem qualifier).
-// A release.cluster arrive cost about 1000 cycles per use on GB300.
+// The reading (PTX ISA, Tensor Core 5th generation chapter):
+//   - "Memory Consistency Model for 5th generation of TensorCore operations",
+//     subsections on specialized inter-thread synchronization and the canonical
+//     synchronization patterns: tcgen05 operations of two threads are ordered by a
+//     thread synchronization bracketed by tcgen05.fence::before_thread_sync in the
+//     signalling thread and tcgen05.fence::after_thread_sync in the waiting one;
+//   - tcgen05.fence: the fences order tcgen05 operations against the thread's
+//     execution-ordering instructions, a class that includes mbarrier arrive and
+//     test_wait / try_wait whatever their .sem qualifier;
+//   - mbarrier.arrive: the .release / .relaxed qualifier gives the ordering of the
+//     arriving thread's memory accesses, which here are none that the waiter reads.
+// So wait::st (or wait::ld), fence::before_thread_sync, this relaxed arrive, the
+// waiter's acquire try_wait and fence::after_thread_sync before its tcgen05.mma order
+// the TMEM stores (reads) before the MMA.  A release.cluster arrive cost about 1000
+// cycles per use on GB300.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
