@@ -149,7 +149,7 @@ struct DensePlan {
 // would keep fewer than half of the SMs busy: 1024^3 FP16 7.0 us against 12.6 us split
 // in clusters); otherwise whichever of the
 // 128 x 256 and 128 x 128 single-CTA instances, each with its own cluster split,
-// moves the fewest bytes per SM (ties: the wider tile).  res256 / res128: resident
+// moves the fewest bytes per SM, the 128 x 128 bytes weighted by 3/4 (below).  res256 / res128: resident
 // clusters per cluster size of the two instances.
 inline DensePlan dense_plan(int64_t M, int64_t N, int64_t K, int k_per_block, int sms, const int* res256,
                             const int* res128) {
@@ -160,7 +160,10 @@ inline DensePlan dense_plan(int64_t M, int64_t N, int64_t K, int k_per_block, in
     const int s128 = choose_split(t128, nkb, sms, res128);
     if (K <= 1024 && 2 * t256 < sms) return DensePlan{DENSE_SINGLE_64, 1};
     const long long b256 = plan_bytes(t256, nkb, 256, s256, sms), b128 = plan_bytes(t128, nkb, 128, s128, sms);
-    return b128 < b256 ? DensePlan{DENSE_SINGLE_128, s128} : DensePlan{DENSE_SINGLE_256, s256};
+    // The 128 x 128 instance's stages hold two boxes of K (8 MMAs per barrier wait and
+    // commit), so it moves its bytes faster: it is taken up to 4/3 of the 128 x 256 bytes
+    // (1024^2 x 4096 FP16 13.6 -> 12.6 us, 128 x 8192^2 28.7 -> 26.9 us).
+    return 3 * b128 < 4 * b256 ? DensePlan{DENSE_SINGLE_128, s128} : DensePlan{DENSE_SINGLE_256, s256};
 }
 
 // ------------------------------------------------------------------ tile raster

@@ -57,10 +57,10 @@ PLAN_CASES = [
     ((2048, 2048, 1024, 64), (SINGLE256, 1)),     # 64 pair tiles, short K: single CTAs (9.4 against 9.8)
     ((512, 8192, 2048, 64), (PAIR256, 1)),        # 64 pair tiles, long K: 17.5 -> 15.7 on pairs
     ((2048, 2048, 4096, 64), (PAIR256, 1)),       # 27.2 -> 24.4 on pairs
-    ((1024, 1024, 4096, 64), (SINGLE256, 4)),     # 20.3 -> 14.4
-    ((256, 2048, 8192, 64), (SINGLE256, 8)),      # 24.9 -> 16.5
-    ((128, 4096, 4096, 64), (SINGLE256, 8)),      # 26.8 -> 12.2
-    ((128, 8192, 8192, 64), (SINGLE256, 4)),      # 37.6 -> 30.3
+    ((1024, 1024, 4096, 64), (SINGLE128, 2)),     # 20.3 -> 14.4; 12.6 on 128 x 128 tiles
+    ((256, 2048, 8192, 64), (SINGLE128, 4)),      # 24.9 -> 16.5 -> 14.7
+    ((128, 4096, 4096, 64), (SINGLE128, 4)),      # 26.8 -> 12.2 -> 11.0
+    ((128, 8192, 8192, 64), (SINGLE128, 2)),      # 37.6 -> 30.3 -> 26.9
     ((128, 2560, 16384, 64), (SINGLE128, 6)),     # 34.2 -> 22.4
     ((500, 760, 16384, 64), (SINGLE128, 6)),      # 31.3 -> 22.2
     ((8192, 8192, 8192, 128), (PAIR256, 1)),

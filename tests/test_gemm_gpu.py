@@ -264,11 +264,11 @@ def test_split_fp16_integers_bit_exact(M, N, K, with_c):
 
 
 # The reduction cuts each CTA's owned chunks into 1, 2 or 4 column parts, as the
-# cluster size leaves room: clusters of 3 (6 or 5 owned 32 x 64 chunks of a 128 x 256
-# tile: whole chunks per warp), 6 (3 or 2: halves), 8 (2: quarters) and, on 128 x 128
-# tiles, 8 (1: quarters, half the warps idle).  The expected cluster sizes are the
-# dispatch rules' on a 152-SM device.
-@pytest.mark.parametrize("M,N,K,split", [(512, 2560, 8192, 3), (256, 2560, 16384, 6), (128, 4096, 4096, 8),
+# cluster size leaves room: clusters of 3 over 128 x 256 tiles (6 or 5 owned 32 x 64
+# chunks: whole chunks per warp), and over 128 x 128 tiles clusters of 3 (3 or 2:
+# halves), 4 (2: quarters) and 8 (1: quarters, half the warps idle).  The expected
+# cluster sizes are the dispatch rules' on a 152-SM device.
+@pytest.mark.parametrize("M,N,K,split", [(512, 2560, 8192, 3), (256, 2560, 16384, 3), (128, 4096, 4096, 4),
                                          (200, 1000, 32768, 8)])
 def test_split_reduce_parts_fp16_integers_bit_exact(M, N, K, split):
     sms = torch.cuda.get_device_properties(P.device()).multi_processor_count
