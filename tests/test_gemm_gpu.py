@@ -280,6 +280,18 @@ def test_split_reduce_parts_fp16_integers_bit_exact(M, N, K, split):
     P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 32, seed=7), mode="exact")
 
 
+# Stages of two 128-byte boxes of K: when K ends inside a stage, its second box lies
+# partly (K = 8200: 8 of 64 elements) or wholly (K = 16448, 32840, 4160) past the end of
+# K and is zero-filled; the split shares count whole stages.
+@pytest.mark.parametrize("M,N,K", [(128, 2560, 16448), (200, 1000, 32840), (1024, 1024, 4160), (384, 520, 8200)])
+def test_split_two_box_stages_ragged_k_bit_exact(M, N, K):
+    sms = torch.cuda.get_device_properties(P.device()).multi_processor_count
+    plan = P.dispatch_plan(M, N, K, 64, sms)
+    assert plan[3] == 2 and plan[4] > 1, "not a split launch on 128 x 128 tiles"
+    prob = inputs.make_problem("f16", M, N, K, seed=M + 3 * N + K, dist="int2", with_c=True)
+    P.check(prob, P.run_gpu(prob, accum=0), rows=P.sample_rows(M, 24, seed=9), mode="exact")
+
+
 def test_split_fp16_in_place():
     prob = inputs.make_problem("f16", 300, 520, 16384, seed=21, dist="int2", with_c=True)
     g = P.to_device(prob, P.device())
