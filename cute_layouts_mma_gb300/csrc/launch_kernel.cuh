@@ -67,10 +67,12 @@ constexpr dispatch::TileShape tile_shape() {
     return dispatch::TileShape{Cfg::BM_TILE, Cfg::BN, Cfg::PAIR, Cfg::kStreamK};
 }
 
+// The rule counts 128-byte k-blocks (kSub of them per stage); the schedule itself
+// deals stages.
 template <class Cfg>
 Schedule choose_schedule(const Params& p, int max_units) {
-    return dispatch::choose_schedule(static_cast<long long>(p.num_m_blocks) * p.num_n_blocks, p.num_k_blocks,
-                                     max_units, Cfg::kStreamK);
+    return dispatch::choose_schedule(static_cast<long long>(p.num_m_blocks) * p.num_n_blocks,
+                                     p.num_k_blocks * Cfg::kSub, max_units, Cfg::kStreamK);
 }
 
 template <class Cfg>
